@@ -1,0 +1,191 @@
+"""CPU oracle for the BASP / Ulysses sequence<->head re-layout.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg may import this package.  The product
+library never imports, links or calls it, and it imports nothing from the
+product package.
+
+Two forms of the same definition live here:
+
+* ``seq2head`` / ``head2seq``: the plain element loop in ``basp_oracle.c``
+  (source-driven; one ``memcpy`` of ``esz`` bytes per element), reached through
+  ctypes.  It is the oracle the parity tests and the CPU baseline use.
+* ``seq2head_by_slices`` / ``head2seq_by_slices``: the same definition written
+  with numpy slicing of the logical tensor ``X[B, S, H, d]``: rebuild ``X``
+  from the shards of one layout, cut it into the shards of the other.
+
+What the layouts are (review "BASP: Communication-Efficient Batch-Aware
+Sequence Parallelism for LLM Training", evolve.pub, sections "Summary",
+"Strengths" and FAQ "What is Batch-Aware Sequence Parallelism (BASP)?"; the
+fugumt.com related-papers entry "DeepSpeed Ulysses"):
+
+* N ranks form G = N/K contiguous groups of K ranks; group g owns sequences
+  ``g*Bg .. g*Bg+Bg-1`` with Bg = B/G.  BASP is K = N/B (Bg = 1, one sequence
+  per group); Ulysses is K = N (one group owning all B sequences).
+* seq-sharded: member j of group g holds tokens ``j*S/K .. (j+1)*S/K - 1`` of
+  all H heads, stored ``[Bg, S/K, H, d]``.
+* head-sharded: member j' holds all S tokens of heads
+  ``j'*H/K .. (j'+1)*H/K - 1``, stored ``[Bg, S, H/K, d]``.
+* Each rank shard has B*S*H*d/N elements in both layouts; shards lie back to
+  back in rank order.
+
+The elements are opaque words: pass any numpy dtype (bf16 travels as uint16).
+The result is a bit copy, so tests compare raw bits.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "basp_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libbasp_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``basp_oracle.c`` with gcc into ``libbasp_oracle.so``."""
+    if force or not os.path.exists(_LIB_PATH) or (
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+        tmp = _LIB_PATH + ".tmp%d" % os.getpid()
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
+                        "-o", tmp, _SRC], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        i64 = ctypes.c_int64
+        for name in ("basp_oracle_seq2head", "basp_oracle_head2seq"):
+            fn = getattr(lib, name)
+            fn.argtypes = [i64] * 7 + [ctypes.c_void_p, ctypes.c_void_p]
+            fn.restype = ctypes.c_int
+        fn = lib.basp_oracle_head_to_seq_index
+        fn.argtypes = [i64] * 7
+        fn.restype = i64
+        _lib = lib
+    return _lib
+
+
+def groups(N: int, K: int, B: int):
+    """Return (G, Bg): number of groups and sequences per group."""
+    G = N // K
+    return G, B // G
+
+
+def valid_shape(B, S, H, d, N, K) -> bool:
+    """The divisibility rules the layouts need (review FAQ "What are BASP's
+    main limitations?": N must be a multiple of the group count's batch split,
+    heads must divide evenly across group members)."""
+    if min(N, K, H, d) < 1 or B < 0 or S < 0:
+        return False
+    if N % K or (B % (N // K)) or S % K or H % K:
+        return False
+    return True
+
+
+def _run(fn_name, x, B, S, H, d, N, K):
+    x = np.ascontiguousarray(x)
+    n = B * S * H * d
+    if x.size != n:
+        raise ValueError("input has %d elements, shape needs %d" % (x.size, n))
+    out = np.empty_like(x)
+    if n == 0:
+        return out
+    rc = getattr(_load(), fn_name)(B, S, H, d, N, K, x.itemsize,
+                                   x.ctypes.data, out.ctypes.data)
+    if rc != 0:
+        raise ValueError("shape breaks a divisibility rule")
+    return out
+
+
+def seq2head(x, B, S, H, d, N, K):
+    """seq-sharded buffer (N shards of [Bg, S/K, H, d]) -> head-sharded buffer
+    (N shards of [Bg, S, H/K, d]).  Plain C element loop."""
+    return _run("basp_oracle_seq2head", x, B, S, H, d, N, K)
+
+
+def head2seq(x, B, S, H, d, N, K):
+    """Inverse of :func:`seq2head`.  Plain C element loop."""
+    return _run("basp_oracle_head2seq", x, B, S, H, d, N, K)
+
+
+def head_to_seq_index(B, S, H, d, N, K, o):
+    """Flat index in the seq-sharded buffer of the element that sits at flat
+    index ``o`` of the head-sharded buffer (destination-driven form)."""
+    r = _load().basp_oracle_head_to_seq_index(B, S, H, d, N, K, int(o))
+    if r < 0:
+        raise ValueError("bad shape or index")
+    return r
+
+
+# ---------------------------------------------------------------------------
+# The definition through the logical tensor X[B, S, H, d] (numpy slicing).
+# ---------------------------------------------------------------------------
+
+def shard_seq(X, N, K):
+    """Cut X[B, S, H, d] into the seq-sharded buffer (flat, rank order)."""
+    B, S, H, d = X.shape
+    G, Bg = groups(N, K, B)
+    Sk = S // K
+    parts = []
+    for r in range(N):
+        g, j = divmod(r, K)
+        parts.append(X[g * Bg:(g + 1) * Bg, j * Sk:(j + 1) * Sk].reshape(-1))
+    return np.concatenate(parts) if parts else X.reshape(-1)
+
+
+def shard_head(X, N, K):
+    """Cut X[B, S, H, d] into the head-sharded buffer (flat, rank order)."""
+    B, S, H, d = X.shape
+    G, Bg = groups(N, K, B)
+    Hk = H // K
+    parts = []
+    for r in range(N):
+        g, jp = divmod(r, K)
+        parts.append(X[g * Bg:(g + 1) * Bg, :, jp * Hk:(jp + 1) * Hk].reshape(-1))
+    return np.concatenate(parts) if parts else X.reshape(-1)
+
+
+def unshard_seq(x, B, S, H, d, N, K):
+    """Rebuild X[B, S, H, d] from a seq-sharded buffer."""
+    G, Bg = groups(N, K, B)
+    Sk = S // K
+    X = np.empty((B, S, H, d), dtype=x.dtype)
+    P = Bg * Sk * H * d
+    for r in range(N):
+        g, j = divmod(r, K)
+        X[g * Bg:(g + 1) * Bg, j * Sk:(j + 1) * Sk] = \
+            x[r * P:(r + 1) * P].reshape(Bg, Sk, H, d)
+    return X
+
+
+def unshard_head(x, B, S, H, d, N, K):
+    """Rebuild X[B, S, H, d] from a head-sharded buffer."""
+    G, Bg = groups(N, K, B)
+    Hk = H // K
+    X = np.empty((B, S, H, d), dtype=x.dtype)
+    P = Bg * S * Hk * d
+    for r in range(N):
+        g, jp = divmod(r, K)
+        X[g * Bg:(g + 1) * Bg, :, jp * Hk:(jp + 1) * Hk] = \
+            x[r * P:(r + 1) * P].reshape(Bg, S, Hk, d)
+    return X
+
+
+def seq2head_by_slices(x, B, S, H, d, N, K):
+    if not valid_shape(B, S, H, d, N, K):
+        raise ValueError("shape breaks a divisibility rule")
+    return shard_head(unshard_seq(x, B, S, H, d, N, K), N, K)
+
+
+def head2seq_by_slices(x, B, S, H, d, N, K):
+    if not valid_shape(B, S, H, d, N, K):
+        raise ValueError("shape breaks a divisibility rule")
+    return shard_seq(unshard_head(x, B, S, H, d, N, K), N, K)
