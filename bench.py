@@ -1,0 +1,549 @@
+"""Benchmark of the seq<->head re-layout (BASP and Ulysses) on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic
+attention activations: Q, K, V seq-sharded -> head-sharded (one call) and the
+attention output O head-sharded -> seq-sharded (one call), through the C ABI.
+GB/s counts algorithmic bytes: every element read once and written once,
+2 * (bytes of Q + K + V + O) per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                    [--layout basp|ulysses] [--algo fused|three_pass]
+                    [--impl ours|reference]
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs an
+independent replica on its own GPU (the path has no cross-GPU step on one
+box); ``value`` is all ranks' bytes over the slowest rank's time.
+``--impl reference`` times the CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("seq↔head re-layout GB/s (read+write) and % of GB300 HBM peak, "
+          "BASP vs Ulysses")
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+KERNEL_SOURCE = os.path.join(ROOT, "sequence_re_layout_gb300", "csrc", "relayout.cu")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--config", default=None)
+    p.add_argument("--layout", default="basp", choices=["basp", "ulysses"])
+    p.add_argument("--algo", default="fused", choices=["fused", "three_pass"])
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--soak-s", type=float, default=1.0,
+                   help="untimed seconds at full load before the timed region "
+                        "(so the clock samples see the loaded GPU)")
+    p.add_argument("--cpu-baseline-s", type=float, default=10.0)
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the Ulysses / three-pass / e2e / CPU legs")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only: barrier and max-reduce on the host)
+# ---------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("gloo", rank=self.rank, world_size=self.world)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, ncu traffic
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        v = d.get("hbm_gbs")
+        if isinstance(v, dict):
+            v = v.get("value")
+        if v:
+            return float(v), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+             "sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index),
+                 "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": "nvidia-smi unavailable"}
+        rows = []
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[3], parts[5:9]))
+            except ValueError:
+                continue
+        win = [r for r in rows if t0 <= r[0] <= t1]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0, "note": "no sample inside the window"}
+        reasons = sorted({n for r in win for n, v in zip(self.NAMES, r[4])
+                          if v.lower().startswith("active")})
+        power = []
+        for r in win:
+            try:
+                power.append(float(r[3]))
+            except ValueError:
+                pass
+        return {"sm_mhz": statistics.median(r[1] for r in win),
+                "sm_max_mhz": max(r[2] for r in win),
+                "reasons": reasons, "samples": len(win),
+                "power_w_median": statistics.median(power) if power else None,
+                "window": "pre-timed soak at the same load + timed region"}
+
+
+def source_digest():
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, layout: str, kernel_role: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return None
+    digest = source_digest()
+    for l in lines:
+        tok = l.split()
+        if len(tok) >= 5 and tok[0] == "traffic" and tok[1] == workload \
+                and tok[2] == layout and tok[3] == kernel_role:
+            kv = dict(t.split("=", 1) for t in tok[4:] if "=" in t)
+            if kv.get("source") != digest:
+                return None
+            return float(kv["bytes"])
+    return None
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def _alloc_sets(w, K, dtype, n_sets, dev, seed):
+    import torch
+    import synth_inputs
+    nq, nkv = w.tensor_elems(w.Hq), w.tensor_elems(w.Hkv)
+    base = [synth_inputs.normal(n, seed + i, dtype).to(dev)
+            for i, n in enumerate((nq, nkv, nkv, nq))]
+    sets = []
+    for s in range(n_sets):
+        ins = base if s == 0 else [t.clone() for t in base]
+        outs = [torch.empty_like(t) for t in ins]
+        sets.append((ins, outs))
+    return sets
+
+
+def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, sampler_cb=None):
+    """Time `steps` steps of the hot path; returns a dict of timings."""
+    import torch
+    import sequence_re_layout_gb300 as basp
+
+    K = w.K(layout)
+    L = basp.Layout(w.B, w.S, w.Hq, w.Hkv, w.d, w.N, K, w.dtype)
+    info = L.info
+    T = info["bytes_q"] * 2 + info["bytes_kv"] * 2            # Q, K, V, O
+    step_bytes = 2 * T
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sets = min(4096, max(2, -(-4 * l2 // step_bytes) + 1))   # >= 4x L2 per rotation
+    sets = _alloc_sets(w, K, w.dtype, n_sets, dev, 1234)
+    ws = None
+    if algo == "three_pass":
+        ws = torch.empty(info["workspace_bytes"], dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        ins, outs = sets[i % n_sets]
+        if ev is not None:
+            ev[0].record(stream)
+        basp.basp_seq2head(L.handle, algo, ins[0], ins[1], ins[2],
+                           outs[0], outs[1], outs[2], ws, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        basp.basp_head2seq(L.handle, algo, ins[3], None, None,
+                           outs[3], None, None, ws, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    soak_t0 = time.time()
+    if soak_s > 0:
+        i = 0
+        while time.time() - soak_t0 < soak_s:
+            for _ in range(50):
+                step(i)
+                i += 1
+            torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+           for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    start.record(stream)
+    for i in range(steps):
+        step(i, evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    total_ms = start.elapsed_time(end)
+    s2h = [e[0].elapsed_time(e[1]) for e in evs]
+    h2s = [e[1].elapsed_time(e[2]) for e in evs]
+    launches_per_step = 2 if algo == "fused" else 6
+    res = {
+        "total_ms": total_ms, "ms_per_step": total_ms / steps,
+        "step_bytes": step_bytes, "info": info, "n_sets": n_sets,
+        "l2_bytes": l2, "s2h_ms_mean": statistics.mean(s2h),
+        "h2s_ms_mean": statistics.mean(h2s),
+        "s2h_bytes": 2 * (info["bytes_q"] + 2 * info["bytes_kv"]),
+        "h2s_bytes": 2 * info["bytes_q"], "launches": launches_per_step * steps,
+        "wall": (soak_t0 if soak_s > 0 else t0, t1),
+    }
+    del sets, ws
+    L.close()
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_e2e(w, layout, algo, steps, warmup, dev):
+    """Same step through the host-buffer C-ABI calls: pinned host inputs are
+    copied in, re-laid out, and copied back out inside the timed region."""
+    import torch
+    import synth_inputs
+    import sequence_re_layout_gb300 as basp
+
+    K = w.K(layout)
+    L = basp.Layout(w.B, w.S, w.Hq, w.Hkv, w.d, w.N, K, w.dtype)
+    info = L.info
+    nq, nkv = w.tensor_elems(w.Hq), w.tensor_elems(w.Hkv)
+    hin = [synth_inputs.normal(n, 1234 + i, w.dtype).pin_memory()
+           for i, n in enumerate((nq, nkv, nkv, nq))]
+    hout = [torch.empty_like(t).pin_memory() for t in hin]
+    staging = torch.empty(info["staging_bytes"], dtype=torch.uint8, device=dev)
+    ws = None
+    if algo == "three_pass":
+        ws = torch.empty(info["workspace_bytes"], dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        basp.basp_seq2head_host(L.handle, algo, hin[0], hin[1], hin[2],
+                                hout[0], hout[1], hout[2], staging,
+                                workspace=ws, stream=stream)
+        basp.basp_head2seq_host(L.handle, algo, hin[3], None, None, hout[3],
+                                None, None, staging, workspace=ws, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = start.elapsed_time(end) / steps
+    T = sum(t.numel() * t.element_size() for t in hin)
+    L.close()
+    return {"ms_per_step": ms, "bytes_in": T, "bytes_out": T, "step_bytes": 2 * T}
+
+
+def cpu_baseline(w, layout, budget_s):
+    """The oracle as it stands (plain C loop, one thread) on the host cores,
+    over whole steps of the same workload, repeated until `budget_s`."""
+    import oracle
+    import synth_inputs
+    oracle.build()
+    K = w.K(layout)
+    nq, nkv = w.tensor_elems(w.Hq), w.tensor_elems(w.Hkv)
+    q, k, v, o = (synth_inputs.bits(synth_inputs.normal(n, 1234 + i, w.dtype))
+                  for i, n in enumerate((nq, nkv, nkv, nq)))
+    step_bytes = 2 * (q.nbytes + k.nbytes + v.nbytes + o.nbytes)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.seq2head(q, w.B, w.S, w.Hq, w.d, w.N, K)
+        oracle.seq2head(k, w.B, w.S, w.Hkv, w.d, w.N, K)
+        oracle.seq2head(v, w.B, w.S, w.Hkv, w.d, w.N, K)
+        oracle.head2seq(o, w.B, w.S, w.Hq, w.d, w.N, K)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": round(step_bytes * reps / el / 1e9, 3), "unit": "GB/s",
+            "cores": 1, "kind": "oracle",
+            "sample": "%d whole steps of %s (%s, Q/K/V seq2head + O head2seq), "
+                      "%.1f s" % (reps, w.name, layout, el)}
+
+
+def gbs(nbytes, ms):
+    return nbytes / (ms * 1e-3) / 1e9
+
+
+def main_ours(args, dist):
+    import torch
+    import sequence_re_layout_gb300 as basp
+    from sequence_re_layout_gb300.build import build_library
+    from sequence_re_layout_gb300.workloads import HEADLINE, WORKLOADS
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path)")
+    build_library() if dist.rank == 0 else None
+    dist.barrier()
+    basp.load_library()
+    dev = torch.device("cuda", dist.local_rank % torch.cuda.device_count())
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.config or HEADLINE]
+    peak, peak_kind = hbm_peak()
+
+    sampler = ClockSampler(dev.index)
+    dist.barrier()
+    r = run_device(w, args.layout, args.algo, args.steps, args.warmup, dev,
+                   soak_s=args.soak_s)
+    sampler.stop()
+    dist.barrier()
+    t_max = dist.max(r["total_ms"])
+    total_bytes = dist.sum(r["step_bytes"] * args.steps)
+    value = total_bytes / (t_max * 1e-3) / 1e9
+    clocks = sampler.summary(*r["wall"])
+
+    info = r["info"]
+    s2h_gbs = gbs(r["s2h_bytes"], r["s2h_ms_mean"])
+    traffic = ncu_traffic(w.name, args.layout, "seq2head_qkv_" + args.algo)
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t_max / args.steps, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (~N(0,1) %s, seeded)" % w.dtype,
+        "config": {
+            "workload": w.name, "layout": args.layout, "algo": args.algo,
+            "B": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "N": w.N,
+            "K": info["K"], "groups": info["groups"],
+            "bytes_per_step": r["step_bytes"],
+            "l2": "inputs rotate over %d buffer sets (%.0f MB per rotation, "
+                  "L2 %.0f MB)" % (r["n_sets"], r["n_sets"] * r["step_bytes"] / 1e6,
+                                   r["l2_bytes"] / 1e6),
+            "parallelism": "replicas" if dist.world > 1 else "single GPU, %d virtual ranks" % w.N,
+        },
+        "pct_hbm_peak": round(100 * value / dist.world / peak, 2),
+        "pct_hbm_nominal": round(100 * value / dist.world / NOMINAL_HBM_GBS, 2),
+        "roofline": {
+            "bound": "hbm", "kernel": "basp_relayout_kernel<16> (seq2head Q,K,V)",
+            "achieved": round(s2h_gbs, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(s2h_gbs / peak, 4), "traffic": traffic,
+            "algorithmic_bytes_per_launch": r["s2h_bytes"],
+            "launch_ms_mean": round(r["s2h_ms_mean"], 6),
+            "peak_kind": "of %s" % peak_kind,
+        },
+        "head2seq": {"achieved_gbs": round(gbs(r["h2s_bytes"], r["h2s_ms_mean"]), 2),
+                     "launch_ms_mean": round(r["h2s_ms_mean"], 6)},
+        "analytic": {"peers_per_rank": info["peers"],
+                     "bytes_per_peer_q": info["bytes_per_peer_q"],
+                     "bytes_per_peer_kv": info["bytes_per_peer_kv"],
+                     "tokens_per_rank": info["tokens_per_rank"],
+                     "foil_tokens_per_rank": info["foil_tokens_per_rank"]},
+        "gpu_launches": r["launches"],
+        "clocks": clocks,
+    }
+    if not args.no_extras and dist.rank == 0:
+        other = "ulysses" if args.layout == "basp" else "basp"
+        ru = run_device(w, other, args.algo, args.steps, args.warmup, dev)
+        vu = gbs(ru["step_bytes"] * args.steps, ru["total_ms"])
+        ou = ru["info"]
+        out[other] = {"value": round(vu, 2), "ms_per_step": round(ru["ms_per_step"], 6),
+                      "K": ou["K"], "pct_hbm_peak": round(100 * vu / peak, 2),
+                      "peers_per_rank": ou["peers"],
+                      "bytes_per_peer_q": ou["bytes_per_peer_q"],
+                      "seq2head_gbs": round(gbs(ru["s2h_bytes"], ru["s2h_ms_mean"]), 2)}
+        alt = "three_pass" if args.algo == "fused" else "fused"
+        rt = run_device(w, args.layout, alt, args.steps, args.warmup, dev)
+        vt = gbs(rt["step_bytes"] * args.steps, rt["total_ms"])
+        out[alt] = {"value": round(vt, 2), "ms_per_step": round(rt["ms_per_step"], 6),
+                    "pct_hbm_peak": round(100 * vt / peak, 2),
+                    "note": "same algorithmic bytes; the three passes move them 3x"}
+        out["gpu_launches"] += ru["launches"] + rt["launches"]
+        e = run_e2e(w, args.layout, args.algo, max(3, min(args.steps, 50)),
+                    3, dev)
+        out["e2e"] = {"value": round(gbs(e["step_bytes"], e["ms_per_step"]), 2),
+                      "unit": "GB/s", "h2d_bytes_per_step": e["bytes_in"],
+                      "d2h_bytes_per_step": e["bytes_out"],
+                      "ms_per_step": round(e["ms_per_step"], 4),
+                      "api": "basp_seq2head_host + basp_head2seq_host (pinned host buffers)"}
+        out["gpu_launches"] += 2 * max(3, min(args.steps, 50)) * (1 if args.algo == "fused" else 3)
+        if dist.world == 1:
+            out["cpu_baseline"] = cpu_baseline(w, args.layout, args.cpu_baseline_s)
+    if dist.rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def main_reference(args, dist):
+    """The reference arm: the CPU oracle, as it stands, timed on the host
+    cores over bounded samples of the same workload (rank 0 only)."""
+    if dist.rank != 0:
+        return
+    import oracle
+    import synth_inputs
+    from sequence_re_layout_gb300.workloads import HEADLINE, WORKLOADS
+    oracle.build()
+    w = WORKLOADS[args.config or HEADLINE]
+    K = w.K(args.layout)
+    # bound the whole run to about two minutes: shrink S (a multiple of K) so
+    # one step takes at most budget / (steps + warmup)
+    budget_s = 120.0
+    nq, nkv = w.tensor_elems(w.Hq), w.tensor_elems(w.Hkv)
+
+    def make(S):
+        ws = [w.B * S * h * w.d for h in (w.Hq, w.Hkv, w.Hkv, w.Hq)]
+        return [synth_inputs.bits(synth_inputs.normal(n, 1234 + i, w.dtype))
+                for i, n in enumerate(ws)]
+
+    def one(S, x):
+        oracle.seq2head(x[0], w.B, S, w.Hq, w.d, w.N, K)
+        oracle.seq2head(x[1], w.B, S, w.Hkv, w.d, w.N, K)
+        oracle.seq2head(x[2], w.B, S, w.Hkv, w.d, w.N, K)
+        oracle.head2seq(x[3], w.B, S, w.Hq, w.d, w.N, K)
+
+    S = w.S
+    probe_S = max(K, (w.S // 16) // K * K)
+    xp = make(probe_S)
+    t0 = time.perf_counter()
+    one(probe_S, xp)
+    per_token = (time.perf_counter() - t0) / probe_S
+    per_step_budget = budget_s / max(1, args.steps + args.warmup)
+    if per_token * w.S > per_step_budget:
+        S = max(K, int(per_step_budget / per_token) // K * K)
+    x = make(S)
+    for _ in range(args.warmup):
+        one(S, x)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one(S, x)
+    el = time.perf_counter() - t0
+    step_bytes = 2 * sum(a.nbytes for a in x)
+    value = step_bytes * args.steps / el / 1e9
+    sample = ("%s at S=%d of %d (same B, heads, d, N, K), %d steps, %.1f s"
+              % (w.name, S, w.S, args.steps, el))
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3),
+        "unit": "GB/s", "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (~N(0,1) %s, seeded)" % w.dtype,
+        "config": {"workload": w.name, "layout": args.layout, "algo": "oracle",
+                   "B": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                   "N": w.N, "K": K},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "GB/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            main_reference(args, dist)
+        else:
+            main_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+"""ctypes binding of ``libbasp.so`` (declared in ``include/basp.h``).
+
+Argument marshalling only: every function here takes Python ints or torch
+tensors, turns them into the C-ABI's pointers and sizes, calls the library and
+raises :class:`BaspError` on a non-OK status.  The re-layout itself runs in the
+library's CUDA kernels; there is no other implementation behind these names.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libbasp.so")
+
+# enums of basp.h
+BASP_DTYPE_BF16, BASP_DTYPE_FP32, BASP_DTYPE_FP16 = 0, 1, 2
+BASP_ALGO_FUSED, BASP_ALGO_THREE_PASS = 0, 1
+(BASP_OK, BASP_ERR_INVALID_ARG, BASP_ERR_DIVISIBILITY, BASP_ERR_BATCH_GT_RANKS,
+ BASP_ERR_ALIGNMENT, BASP_ERR_ALIASING, BASP_ERR_WORKSPACE, BASP_ERR_CUDA,
+ BASP_ERR_TOO_LARGE) = range(9)
+
+DTYPE_CODES = {"bf16": BASP_DTYPE_BF16, "fp32": BASP_DTYPE_FP32,
+               "fp16": BASP_DTYPE_FP16}
+ALGO_CODES = {"fused": BASP_ALGO_FUSED, "three_pass": BASP_ALGO_THREE_PASS}
+
+# every symbol include/basp.h declares
+EXPORTS = ("basp_layout_create", "basp_layout_query", "basp_layout_destroy",
+           "basp_seq2head", "basp_head2seq", "basp_seq2head_host",
+           "basp_head2seq_host", "basp_status_string")
+
+
+class basp_info(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "B", "S", "Hq", "Hkv", "d", "N", "K", "groups", "seqs_per_group",
+        "tokens_per_rank", "elem_size", "elems_per_rank_q", "elems_per_rank_kv",
+        "peers", "bytes_per_peer_q", "bytes_per_peer_kv", "bytes_q", "bytes_kv",
+        "workspace_bytes", "staging_bytes", "foil_tokens_per_rank")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class BaspError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, basp_status_string(status), status))
+
+
+_lib = None
+
+
+def load_library():
+    """Load the in-tree ``libbasp.so``.  There is no fallback: a missing
+    library is an error."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            "libbasp.so is not built (expected at %s); run "
+            "sequence_re_layout_gb300.build.build_library()" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    lib.basp_layout_create.argtypes = [i64] * 7 + [ctypes.c_int, ctypes.POINTER(vp)]
+    lib.basp_layout_create.restype = ctypes.c_int
+    lib.basp_layout_query.argtypes = [vp, ctypes.POINTER(basp_info)]
+    lib.basp_layout_query.restype = ctypes.c_int
+    lib.basp_layout_destroy.argtypes = [vp]
+    lib.basp_layout_destroy.restype = None
+    for name in ("basp_seq2head", "basp_head2seq"):
+        fn = getattr(lib, name)
+        fn.argtypes = [vp, ctypes.c_int] + [vp] * 6 + [vp, sz, vp]
+        fn.restype = ctypes.c_int
+    for name in ("basp_seq2head_host", "basp_head2seq_host"):
+        fn = getattr(lib, name)
+        fn.argtypes = [vp, ctypes.c_int] + [vp] * 6 + [vp, sz, vp, sz, vp]
+        fn.restype = ctypes.c_int
+    lib.basp_status_string.argtypes = [ctypes.c_int]
+    lib.basp_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    """A device/host address from None, an int or a tensor."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x or None
+    return x.data_ptr() or None
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s or None
+    return s.cuda_stream or None
+
+
+def _check(status, where):
+    if status != BASP_OK:
+        raise BaspError(status, where)
+
+
+def basp_status_string(status: int) -> str:
+    return load_library().basp_status_string(int(status)).decode()
+
+
+def basp_layout_create(B, S, Hq, Hkv, d, N, K, dtype="bf16") -> int:
+    """Create a layout handle (an opaque int).  ``K = 0`` asks for the BASP
+    rule K = N/B.  ``dtype`` is "bf16", "fp16", "fp32" or the enum value."""
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
+    h = ctypes.c_void_p()
+    _check(load_library().basp_layout_create(B, S, Hq, Hkv, d, N, K, code,
+                                             ctypes.byref(h)),
+           "basp_layout_create")
+    return h.value
+
+
+def basp_layout_query(layout: int) -> dict:
+    info = basp_info()
+    _check(load_library().basp_layout_query(layout, ctypes.byref(info)),
+           "basp_layout_query")
+    return info.as_dict()
+
+
+def basp_layout_destroy(layout: int) -> None:
+    load_library().basp_layout_destroy(layout)
+
+
+def _algo(a):
+    return ALGO_CODES[a] if isinstance(a, str) else int(a)
+
+
+def _nbytes(x):
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return x.numel() * x.element_size()
+
+
+def basp_seq2head(layout, algo, q, k, v, q_out, k_out, v_out,
+                  workspace=None, workspace_bytes=None, stream=None):
+    """seq-sharded -> head-sharded (device buffers); see ``basp.h``."""
+    wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    _check(load_library().basp_seq2head(
+        layout, _algo(algo), _ptr(q), _ptr(k), _ptr(v), _ptr(q_out),
+        _ptr(k_out), _ptr(v_out), _ptr(workspace), wb, _stream(stream)),
+        "basp_seq2head")
+
+
+def basp_head2seq(layout, algo, o, k, v, o_out, k_out, v_out,
+                  workspace=None, workspace_bytes=None, stream=None):
+    """head-sharded -> seq-sharded (device buffers); see ``basp.h``."""
+    wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    _check(load_library().basp_head2seq(
+        layout, _algo(algo), _ptr(o), _ptr(k), _ptr(v), _ptr(o_out),
+        _ptr(k_out), _ptr(v_out), _ptr(workspace), wb, _stream(stream)),
+        "basp_head2seq")
+
+
+def basp_seq2head_host(layout, algo, q, k, v, q_out, k_out, v_out, staging,
+                       staging_bytes=None, workspace=None,
+                       workspace_bytes=None, stream=None):
+    """Host buffers in and out, device ``staging``; see ``basp.h``."""
+    sb = _nbytes(staging) if staging_bytes is None else staging_bytes
+    wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    _check(load_library().basp_seq2head_host(
+        layout, _algo(algo), _ptr(q), _ptr(k), _ptr(v), _ptr(q_out),
+        _ptr(k_out), _ptr(v_out), _ptr(staging), sb, _ptr(workspace), wb,
+        _stream(stream)), "basp_seq2head_host")
+
+
+def basp_head2seq_host(layout, algo, o, k, v, o_out, k_out, v_out, staging,
+                       staging_bytes=None, workspace=None,
+                       workspace_bytes=None, stream=None):
+    """Host buffers in and out, device ``staging``; see ``basp.h``."""
+    sb = _nbytes(staging) if staging_bytes is None else staging_bytes
+    wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    _check(load_library().basp_head2seq_host(
+        layout, _algo(algo), _ptr(o), _ptr(k), _ptr(v), _ptr(o_out),
+        _ptr(k_out), _ptr(v_out), _ptr(staging), sb, _ptr(workspace), wb,
+        _stream(stream)), "basp_head2seq_host")
+
+
+class Layout:
+    """Owns one layout handle; ``info`` holds the derived sizes."""
+
+    def __init__(self, B, S, Hq, Hkv, d, N, K, dtype="bf16"):
+        self.handle = basp_layout_create(B, S, Hq, Hkv, d, N, K, dtype)
+        self.info = basp_layout_query(self.handle)
+
+    def close(self):
+        if self.handle:
+            basp_layout_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

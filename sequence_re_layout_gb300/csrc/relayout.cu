@@ -1,0 +1,515 @@
+// relayout.cu -- the seq-sharded <-> head-sharded re-layout kernels for
+// sm_103a and the C-ABI entry points that plan and launch them.
+//
+// The operation is the all-to-all of Ulysses / BASP attention (review "BASP:
+// Communication-Efficient Batch-Aware Sequence Parallelism for LLM Training",
+// evolve.pub, "Summary" and FAQ "What is Batch-Aware Sequence Parallelism
+// (BASP)?"), done on one GPU where the N ranks are shards of one allocation,
+// so the exchange is a permutation in HBM.
+//
+// Every buffer involved is a set of "rows": contiguous runs of
+// L = (H/K)*d elements (one rank's head block of one token), addressed by five
+// coordinates
+//     g  group                      (G = N/K)
+//     j  member holding the tokens  (K)   -- seq-sharded owner
+//     jp member holding the heads   (K)   -- head-sharded owner
+//     bl sequence within the group  (Bg = B/G)
+//     sl token within the block     (S/K)
+// and each buffer kind is a stride table over them:
+//     SEQ   seq-sharded  [G][K j][Bg][S/K sl][K jp][L]
+//     HEAD  head-sharded [G][K jp][Bg][K j][S/K sl][L]
+//     BYSRC send chunks  [G][K j][K jp][Bg][S/K][L]   (chunk jp of rank g*K+j)
+//     BYDST recv chunks  [G][K jp][K j][Bg][S/K][L]   (slot j of rank g*K+jp)
+// A pass copies every row from one kind to another.  The fused path is one
+// pass SEQ -> HEAD (or back); the three-pass path is pack (SEQ -> BYSRC),
+// exchange (BYSRC -> BYDST, whole chunks), unpack (BYDST -> HEAD).
+//
+// One kernel serves every pass: a persistent grid walks "tiles" of 16-byte
+// vectors; a tile belongs to one "block" (fixed g, j, jp, bl: S/K rows), whose
+// source and destination base offsets come from the two stride tables; inside
+// the block, vector i sits in row i / vpr, column i % vpr (vpr = vectors per
+// row; the division uses the Granlund-Montgomery multiply-high method for
+// invariant divisors, "Division by Invariant Integers using Multiplication",
+// PLDI 1994).  Loads are non-coherent streaming loads that skip L1; each thread
+// keeps kUnroll independent 16-byte loads in flight before it stores.  No
+// shared memory, no tensor cores: the work is pure data movement, bounded by
+// HBM bandwidth.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include "layout_internal.h"
+
+namespace {
+
+constexpr int kThreads = 256;   // threads per CTA
+constexpr int kUnroll = 4;      // vectors in flight per thread
+constexpr int kTileVec = kThreads * kUnroll;
+constexpr int kMaxJobs = 3;
+
+enum Coord { C_G = 0, C_J = 1, C_JP = 2, C_BL = 3, C_SL = 4 };
+enum BufKind { SEQ, HEAD, BYSRC, BYDST };
+
+// One tensor's share of one launch.
+struct Job {
+    const unsigned char *src;
+    unsigned char *dst;
+    int64_t src_bs[4], dst_bs[4];   // block-digit strides, in vectors
+    int64_t src_rs, dst_rs;         // row strides, in vectors
+    uint32_t radix[4];              // block-digit radices; digit 3 fastest
+    uint32_t vpr;                   // vectors per row
+    uint32_t vpr_magic, vpr_shift;  // i / vpr == (umulhi(i, magic) + i) >> shift
+    uint32_t vec_per_block;         // rows * vpr  (< 2^31)
+    uint32_t tiles_per_block;
+    uint32_t tile_begin;            // first tile of this job within the launch
+};
+
+struct Params {
+    Job job[kMaxJobs];
+    int njobs;
+    uint32_t total_tiles;
+};
+
+template <int VEC> struct Word;
+template <> struct Word<16> { using T = uint4; };
+template <> struct Word<8> { using T = uint2; };
+template <> struct Word<4> { using T = uint32_t; };
+template <> struct Word<2> { using T = unsigned short; };
+
+__device__ __forceinline__ uint4 load_stream(const uint4 *p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 load_stream(const uint2 *p) {
+    uint2 v;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+        : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t load_stream(const uint32_t *p) {
+    uint32_t v;
+    asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ unsigned short load_stream(const unsigned short *p) {
+    unsigned short v;
+    asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void store(uint4 *p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ void store(uint2 *p, uint2 v) {
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};"
+                 :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+__device__ __forceinline__ void store(uint32_t *p, uint32_t v) {
+    asm volatile("st.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void store(unsigned short *p, unsigned short v) {
+    asm volatile("st.global.u16 [%0], %1;" :: "l"(p), "h"(v) : "memory");
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kThreads)
+basp_relayout_kernel(const __grid_constant__ Params p) {
+    using W = typename Word<VEC>::T;
+    for (uint32_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        int jb = 0;
+        if (p.njobs > 1 && t >= p.job[1].tile_begin) jb = 1;
+        if (p.njobs > 2 && t >= p.job[2].tile_begin) jb = 2;
+        const Job &J = p.job[jb];
+
+        // tile -> (block, tile within block) -> block digits
+        const uint32_t lt = t - J.tile_begin;
+        uint32_t blk = lt / J.tiles_per_block;
+        const uint32_t tb = lt - blk * J.tiles_per_block;
+        int64_t sb = 0, db = 0;
+#pragma unroll
+        for (int k = 3; k >= 1; --k) {
+            const uint32_t q = blk / J.radix[k];
+            const uint32_t dgt = blk - q * J.radix[k];
+            sb += int64_t(dgt) * J.src_bs[k];
+            db += int64_t(dgt) * J.dst_bs[k];
+            blk = q;
+        }
+        sb += int64_t(blk) * J.src_bs[0];
+        db += int64_t(blk) * J.dst_bs[0];
+
+        const uint32_t i0 = tb * uint32_t(kTileVec);
+        const uint32_t i1 = min(i0 + uint32_t(kTileVec), J.vec_per_block);
+        const W *src = reinterpret_cast<const W *>(J.src) + sb;
+        W *dst = reinterpret_cast<W *>(J.dst) + db;
+
+        W v[kUnroll];
+        int64_t doff[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint32_t i = i0 + threadIdx.x + uint32_t(u * kThreads);
+            if (i < i1) {
+                const uint32_t row = (__umulhi(i, J.vpr_magic) + i) >> J.vpr_shift;
+                const uint32_t col = i - row * J.vpr;
+                v[u] = load_stream(src + (int64_t(row) * J.src_rs + col));
+                doff[u] = int64_t(row) * J.dst_rs + col;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint32_t i = i0 + threadIdx.x + uint32_t(u * kThreads);
+            if (i < i1) store(dst + doff[u], v[u]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side: stride tables, pass planning, launch.
+// ---------------------------------------------------------------------------
+
+// Strides (in vectors) of the five coordinates for one buffer kind.
+void strides_of(const basp_layout &L, BufKind kind, int64_t vpr, int64_t s[5]) {
+    const int64_t K = L.K, Bg = L.Bg, Sk = L.Sk;
+    switch (kind) {
+        case SEQ:     // [G][K j][Bg][Sk][K jp][vpr]
+            s[C_JP] = vpr;
+            s[C_SL] = K * vpr;
+            s[C_BL] = Sk * K * vpr;
+            s[C_J] = Bg * Sk * K * vpr;
+            s[C_G] = K * Bg * Sk * K * vpr;
+            break;
+        case HEAD:    // [G][K jp][Bg][K j][Sk][vpr]
+            s[C_SL] = vpr;
+            s[C_J] = Sk * vpr;
+            s[C_BL] = K * Sk * vpr;
+            s[C_JP] = Bg * K * Sk * vpr;
+            s[C_G] = K * Bg * K * Sk * vpr;
+            break;
+        case BYSRC:   // [G][K j][K jp][Bg][Sk][vpr]
+            s[C_SL] = vpr;
+            s[C_BL] = Sk * vpr;
+            s[C_JP] = Bg * Sk * vpr;
+            s[C_J] = K * Bg * Sk * vpr;
+            s[C_G] = K * K * Bg * Sk * vpr;
+            break;
+        case BYDST:   // [G][K jp][K j][Bg][Sk][vpr]
+            s[C_SL] = vpr;
+            s[C_BL] = Sk * vpr;
+            s[C_J] = Bg * Sk * vpr;
+            s[C_JP] = K * Bg * Sk * vpr;
+            s[C_G] = K * K * Bg * Sk * vpr;
+            break;
+    }
+}
+
+int64_t extent_of(const basp_layout &L, int c) {
+    switch (c) {
+        case C_G: return L.G;
+        case C_J: return L.K;
+        case C_JP: return L.K;
+        case C_BL: return L.Bg;
+        default: return L.Sk;
+    }
+}
+
+// Granlund-Montgomery constants for unsigned 32-bit division by D (1 <= D <
+// 2^31), valid for dividends below 2^31: l = ceil(log2 D),
+// m = floor(2^32 * (2^l - D) / D) + 1, and n / D == (umulhi(n, m) + n) >> l.
+void udiv_magic(uint32_t D, uint32_t *m, uint32_t *l) {
+    uint32_t ll = 0;
+    while ((uint64_t(1) << ll) < D) ++ll;
+    const uint64_t mm = ((uint64_t(1) << 32) * ((uint64_t(1) << ll) - D)) / D + 1;
+    *m = uint32_t(mm);
+    *l = ll;
+}
+
+struct TensorArg {
+    const void *in;
+    void *out;
+    int64_t H;
+};
+
+struct Pass {
+    BufKind from, to;
+    int digit[4];     // block digits, outermost first; the row coordinate is sl
+};
+
+// The passes of each path, the destination's order chosen for the digits so
+// consecutive tiles write consecutive memory.
+constexpr Pass kFusedS2H = {SEQ, HEAD, {C_G, C_JP, C_BL, C_J}};
+constexpr Pass kFusedH2S = {HEAD, SEQ, {C_G, C_J, C_BL, C_JP}};
+constexpr Pass kPackS2H = {SEQ, BYSRC, {C_G, C_J, C_JP, C_BL}};
+constexpr Pass kExchS2H = {BYSRC, BYDST, {C_G, C_JP, C_J, C_BL}};
+constexpr Pass kUnpackS2H = {BYDST, HEAD, {C_G, C_JP, C_BL, C_J}};
+constexpr Pass kPackH2S = {HEAD, BYDST, {C_G, C_JP, C_J, C_BL}};
+constexpr Pass kExchH2S = {BYDST, BYSRC, {C_G, C_J, C_JP, C_BL}};
+constexpr Pass kUnpackH2S = {BYSRC, SEQ, {C_G, C_J, C_BL, C_JP}};
+
+// Widest vector (bytes) that divides the row length and every address.
+int pick_vec(const basp_layout &L, const TensorArg *t, int n,
+             const void *const *extra, int nextra) {
+    int vec = 16;
+    auto fits = [&](uintptr_t x) { return (x % uintptr_t(vec)) == 0; };
+    while (vec > L.esz) {
+        bool ok = true;
+        for (int i = 0; i < n && ok; ++i) {
+            const int64_t row_bytes = (t[i].H / L.K) * L.d * L.esz;
+            ok = fits(uintptr_t(row_bytes)) && fits(uintptr_t(t[i].in)) &&
+                 fits(uintptr_t(t[i].out));
+        }
+        for (int i = 0; i < nextra && ok; ++i) ok = fits(uintptr_t(extra[i]));
+        if (ok) break;
+        vec /= 2;
+    }
+    return vec;
+}
+
+basp_status plan(const basp_layout &L, const Pass &pass, const TensorArg *t,
+                 int n, int vec, Params *p) {
+    std::memset(p, 0, sizeof(*p));
+    uint64_t tiles = 0;
+    int nj = 0;
+    for (int i = 0; i < n; ++i) {
+        const int64_t row_bytes = (t[i].H / L.K) * L.d * L.esz;
+        const int64_t vpr = row_bytes / vec;
+        const int64_t vec_per_block = L.Sk * vpr;
+        if (vec_per_block == 0) continue;                    // empty tensor
+        if (vec_per_block >= (int64_t(1) << 31)) return BASP_ERR_TOO_LARGE;
+        Job &J = p->job[nj++];
+        int64_t ss[5], ds[5];
+        strides_of(L, pass.from, vpr, ss);
+        strides_of(L, pass.to, vpr, ds);
+        for (int k = 0; k < 4; ++k) {
+            J.src_bs[k] = ss[pass.digit[k]];
+            J.dst_bs[k] = ds[pass.digit[k]];
+            J.radix[k] = uint32_t(extent_of(L, pass.digit[k]));
+        }
+        J.src_rs = ss[C_SL];
+        J.dst_rs = ds[C_SL];
+        J.src = static_cast<const unsigned char *>(t[i].in);
+        J.dst = static_cast<unsigned char *>(t[i].out);
+        J.vpr = uint32_t(vpr);
+        udiv_magic(J.vpr, &J.vpr_magic, &J.vpr_shift);
+        J.vec_per_block = uint32_t(vec_per_block);
+        J.tiles_per_block = uint32_t((vec_per_block + kTileVec - 1) / kTileVec);
+        J.tile_begin = uint32_t(tiles);
+        const uint64_t blocks = uint64_t(L.G) * L.K * L.K * L.Bg;
+        tiles += blocks * J.tiles_per_block;
+        if (tiles >= (uint64_t(1) << 31)) return BASP_ERR_TOO_LARGE;
+    }
+    p->njobs = nj;
+    p->total_tiles = uint32_t(tiles);
+    return BASP_OK;
+}
+
+template <int VEC>
+int grid_for(uint32_t tiles) {
+    // Persistent grid: every SM filled to its resident-CTA limit, cached per
+    // device (a benign race: every thread computes the same numbers).
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    int slots = cache[dev].load(std::memory_order_relaxed);
+    if (slots == 0) {
+        int sms = 0, per_sm = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, basp_relayout_kernel<VEC>, kThreads, 0);
+        slots = (sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
+        cache[dev].store(slots, std::memory_order_relaxed);
+    }
+    return int(tiles < uint32_t(slots) ? tiles : uint32_t(slots));
+}
+
+template <int VEC>
+basp_status launch_vec(const Params &p, cudaStream_t stream) {
+    const int grid = grid_for<VEC>(p.total_tiles);
+    basp_relayout_kernel<VEC><<<grid, kThreads, 0, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? BASP_OK : BASP_ERR_CUDA;
+}
+
+basp_status run_pass(const basp_layout &L, const Pass &pass,
+                     const TensorArg *t, int n, int vec, cudaStream_t stream) {
+    Params p;
+    basp_status st = plan(L, pass, t, n, vec, &p);
+    if (st != BASP_OK || p.total_tiles == 0) return st;
+    switch (vec) {
+        case 16: return launch_vec<16>(p, stream);
+        case 8: return launch_vec<8>(p, stream);
+        case 4: return launch_vec<4>(p, stream);
+        default: return launch_vec<2>(p, stream);
+    }
+}
+
+bool overlaps(const void *a, int64_t na, const void *b, int64_t nb) {
+    if (na <= 0 || nb <= 0 || a == nullptr || b == nullptr) return false;
+    const uintptr_t x = uintptr_t(a), y = uintptr_t(b);
+    return x < y + uintptr_t(nb) && y < x + uintptr_t(na);
+}
+
+// Gather the (input, output, heads) triples of one call and check pairing,
+// alignment and aliasing.  `first_H` is Hq (Q or O); the other two are Hkv.
+basp_status collect(const basp_layout *L, const void *a, const void *k,
+                    const void *v, void *ao, void *ko, void *vo,
+                    TensorArg *t, int *n) {
+    if (L == nullptr) return BASP_ERR_INVALID_ARG;
+    const TensorArg all[3] = {{a, ao, L->Hq}, {k, ko, L->Hkv}, {v, vo, L->Hkv}};
+    *n = 0;
+    for (const TensorArg &x : all) {
+        if ((x.in == nullptr) != (x.out == nullptr)) return BASP_ERR_INVALID_ARG;
+        if (x.in != nullptr) t[(*n)++] = x;
+    }
+    if (*n == 0) return BASP_ERR_INVALID_ARG;
+    for (int i = 0; i < *n; ++i) {
+        if (uintptr_t(t[i].in) % uintptr_t(L->esz) ||
+            uintptr_t(t[i].out) % uintptr_t(L->esz))
+            return BASP_ERR_ALIGNMENT;
+    }
+    for (int i = 0; i < *n; ++i) {
+        const int64_t bi = basp::tensor_bytes(*L, t[i].H);
+        for (int j = 0; j < *n; ++j) {
+            const int64_t bj = basp::tensor_bytes(*L, t[j].H);
+            if (overlaps(t[i].out, bi, t[j].in, bj)) return BASP_ERR_ALIASING;
+            if (i != j && overlaps(t[i].out, bi, t[j].out, bj))
+                return BASP_ERR_ALIASING;
+        }
+    }
+    return BASP_OK;
+}
+
+int64_t region_bytes(const basp_layout &L, const TensorArg *t, int n) {
+    int64_t H[3];
+    for (int i = 0; i < n; ++i) H[i] = t[i].H;
+    return basp::workspace_bytes(L, H, n);
+}
+
+basp_status relayout(const basp_layout *L, basp_algo algo, bool to_head,
+                     const void *a, const void *k, const void *v, void *ao,
+                     void *ko, void *vo, void *ws, size_t ws_bytes,
+                     cudaStream_t stream) {
+    TensorArg t[3];
+    int n = 0;
+    basp_status st = collect(L, a, k, v, ao, ko, vo, t, &n);
+    if (st != BASP_OK) return st;
+    if (algo == BASP_ALGO_FUSED) {
+        const int vec = pick_vec(*L, t, n, nullptr, 0);
+        return run_pass(*L, to_head ? kFusedS2H : kFusedH2S, t, n, vec, stream);
+    }
+    if (algo != BASP_ALGO_THREE_PASS) return BASP_ERR_INVALID_ARG;
+
+    const int64_t need = region_bytes(*L, t, n);
+    if (need > 0 && (ws == nullptr || int64_t(ws_bytes) < need))
+        return BASP_ERR_WORKSPACE;
+    for (int i = 0; i < n; ++i) {
+        const int64_t b = basp::tensor_bytes(*L, t[i].H);
+        if (overlaps(ws, need, t[i].in, b) || overlaps(ws, need, t[i].out, b))
+            return BASP_ERR_ALIASING;
+    }
+    if (uintptr_t(ws) % uintptr_t(L->esz)) return BASP_ERR_ALIGNMENT;
+    // workspace regions: [send 0][recv 0][send 1][recv 1]...
+    TensorArg pack[3], exch[3], unpack[3];
+    const void *extra[1] = {ws};
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    for (int i = 0; i < n; ++i) {
+        const int64_t r = basp::align256(basp::tensor_bytes(*L, t[i].H));
+        unsigned char *send = w, *recv = w + r;
+        w += 2 * r;
+        pack[i] = {t[i].in, send, t[i].H};
+        exch[i] = {send, recv, t[i].H};
+        unpack[i] = {recv, t[i].out, t[i].H};
+    }
+    const int vec = pick_vec(*L, t, n, extra, 1);
+    const Pass *passes[3] = {to_head ? &kPackS2H : &kPackH2S,
+                             to_head ? &kExchS2H : &kExchH2S,
+                             to_head ? &kUnpackS2H : &kUnpackH2S};
+    const TensorArg *args[3] = {pack, exch, unpack};
+    for (int s = 0; s < 3; ++s) {
+        st = run_pass(*L, *passes[s], args[s], n, vec, stream);
+        if (st != BASP_OK) return st;
+    }
+    return BASP_OK;
+}
+
+basp_status relayout_host(const basp_layout *L, basp_algo algo, bool to_head,
+                          const void *a, const void *k, const void *v,
+                          void *ao, void *ko, void *vo, void *staging,
+                          size_t staging_bytes, void *ws, size_t ws_bytes,
+                          cudaStream_t stream) {
+    TensorArg t[3];
+    int n = 0;
+    basp_status st = collect(L, a, k, v, ao, ko, vo, t, &n);
+    if (st != BASP_OK) return st;
+    const int64_t need = region_bytes(*L, t, n);
+    if (need > 0 && (staging == nullptr || int64_t(staging_bytes) < need))
+        return BASP_ERR_WORKSPACE;
+    if (overlaps(staging, need, ws, int64_t(ws_bytes))) return BASP_ERR_ALIASING;
+    // staging regions: [in 0][out 0][in 1][out 1]...
+    const void *din[3] = {nullptr, nullptr, nullptr};
+    void *dout[3] = {nullptr, nullptr, nullptr};
+    unsigned char *sp = static_cast<unsigned char *>(staging);
+    for (int i = 0; i < n; ++i) {
+        const int64_t b = basp::tensor_bytes(*L, t[i].H);
+        const int64_t r = basp::align256(b);
+        din[i] = sp;
+        dout[i] = sp + r;
+        sp += 2 * r;
+        if (b > 0 && cudaMemcpyAsync(sp - 2 * r, t[i].in, size_t(b),
+                                     cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return BASP_ERR_CUDA;
+    }
+    // Map the staged buffers back onto the (first, k, v) argument slots.
+    const void *sa[3] = {nullptr, nullptr, nullptr};
+    void *so[3] = {nullptr, nullptr, nullptr};
+    int i = 0;
+    if (a) { sa[0] = din[i]; so[0] = dout[i]; ++i; }
+    if (k) { sa[1] = din[i]; so[1] = dout[i]; ++i; }
+    if (v) { sa[2] = din[i]; so[2] = dout[i]; ++i; }
+    st = relayout(L, algo, to_head, sa[0], sa[1], sa[2], so[0], so[1], so[2],
+                  ws, ws_bytes, stream);
+    if (st != BASP_OK) return st;
+    for (int x = 0; x < n; ++x) {
+        const int64_t b = basp::tensor_bytes(*L, t[x].H);
+        if (b > 0 && cudaMemcpyAsync(t[x].out, dout[x], size_t(b),
+                                     cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+            return BASP_ERR_CUDA;
+    }
+    return BASP_OK;
+}
+
+}  // namespace
+
+extern "C" basp_status basp_seq2head(const basp_layout *L, basp_algo algo,
+                                     const void *q, const void *k, const void *v,
+                                     void *q_out, void *k_out, void *v_out,
+                                     void *ws, size_t ws_bytes, cudaStream_t stream) {
+    return relayout(L, algo, true, q, k, v, q_out, k_out, v_out, ws, ws_bytes, stream);
+}
+
+extern "C" basp_status basp_head2seq(const basp_layout *L, basp_algo algo,
+                                     const void *o, const void *k, const void *v,
+                                     void *o_out, void *k_out, void *v_out,
+                                     void *ws, size_t ws_bytes, cudaStream_t stream) {
+    return relayout(L, algo, false, o, k, v, o_out, k_out, v_out, ws, ws_bytes, stream);
+}
+
+extern "C" basp_status basp_seq2head_host(const basp_layout *L, basp_algo algo,
+                                          const void *q, const void *k, const void *v,
+                                          void *q_out, void *k_out, void *v_out,
+                                          void *staging, size_t staging_bytes,
+                                          void *ws, size_t ws_bytes, cudaStream_t stream) {
+    return relayout_host(L, algo, true, q, k, v, q_out, k_out, v_out, staging,
+                         staging_bytes, ws, ws_bytes, stream);
+}
+
+extern "C" basp_status basp_head2seq_host(const basp_layout *L, basp_algo algo,
+                                          const void *o, const void *k, const void *v,
+                                          void *o_out, void *k_out, void *v_out,
+                                          void *staging, size_t staging_bytes,
+                                          void *ws, size_t ws_bytes, cudaStream_t stream) {
+    return relayout_host(L, algo, false, o, k, v, o_out, k_out, v_out, staging,
+                         staging_bytes, ws, ws_bytes, stream);
+}

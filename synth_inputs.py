@@ -62,3 +62,16 @@ def index_valued(n: int, offset: int = 0) -> torch.Tensor:
 def bits(t: torch.Tensor) -> np.ndarray:
     """Raw bits of a CPU tensor as a numpy integer array."""
     return t.contiguous().view(BITS[t.dtype]).numpy()
+
+
+def random_bits_device(n: int, seed: int, dtype: str, device) -> torch.Tensor:
+    """Like :func:`random_bits`, drawn by the device's own generator (for
+    buffers too large to draw on the CPU in a test's time)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    t = DTYPES[dtype]
+    bt = BITS[t]
+    info = torch.iinfo(bt)
+    x = torch.randint(info.min, info.max + 1, (int(n),), generator=g,
+                      dtype=bt, device=device)
+    return x.view(t)

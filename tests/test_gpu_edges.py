@@ -1,0 +1,171 @@
+"""GPU edge cases: empty shapes, narrower-than-16-byte alignment, guard bands
+around every output, buffers above 2^31 elements, subsets of Q/K/V, streams,
+and the host-buffer entry points."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth_inputs
+import sequence_re_layout_gb300 as basp
+from parity import (assert_bits_equal, device_outputs, make_inputs,
+                    oracle_outputs)
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+ALGOS = ("fused", "three_pass")
+
+
+@pytest.mark.parametrize("shape", [
+    (2, 0, 8, 8, 16, 4, 2),     # S = 0
+    (0, 64, 8, 8, 16, 4, 4),    # B = 0 (Ulysses)
+])
+@pytest.mark.parametrize("algo", ALGOS)
+def test_empty_shapes_launch_nothing(shape, algo):
+    B, S, Hq, Hkv, d, N, K = shape
+    with basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16") as L:
+        assert L.info["bytes_q"] == 0
+        x = torch.empty(8, dtype=torch.bfloat16, device=DEV)
+        y = torch.empty(8, dtype=torch.bfloat16, device=DEV)
+        basp.basp_seq2head(L.handle, algo, x, None, None, y, None, None, None, 0)
+        basp.basp_head2seq(L.handle, algo, x, None, None, y, None, None, None, 0)
+        torch.cuda.synchronize()
+
+
+def _padded(n, dtype, offset_bytes, fill_bits):
+    """A view of n elements starting offset_bytes into a larger buffer whose
+    other bytes hold a sentinel; returns (view, backing bytes)."""
+    esz = torch.tensor([], dtype=dtype).element_size()
+    pad = 4096
+    raw = torch.full((pad + offset_bytes + n * esz + pad,), fill_bits,
+                     dtype=torch.uint8, device=DEV)
+    start = pad + offset_bytes
+    view = raw[start:start + n * esz].view(dtype)
+    return view, raw, start, start + n * esz
+
+
+@pytest.mark.parametrize("offset", [0, 2, 4, 8, 256])
+@pytest.mark.parametrize("algo", ALGOS)
+def test_alignment_fallbacks_and_guard_bands(offset, algo):
+    """Pointers 2/4/8 bytes past a 16-byte boundary take the narrower vector
+    kernels; every byte outside the outputs and the workspace keeps its
+    sentinel."""
+    B, S, Hq, Hkv, d, N, K = 2, 96, 12, 4, 40, 4, 2
+    dtype = "bf16"
+    tdt = synth_inputs.DTYPES[dtype]
+    q, k, v, o = make_inputs(B, S, Hq, Hkv, d, dtype, 5, kind="bits")
+    exp = oracle_outputs(q, k, v, o, B, S, Hq, Hkv, d, N, K)
+    ins, outs, raws = [], [], []
+    for t in (q, k, v, o):
+        xi, _, _, _ = _padded(t.numel(), tdt, offset, 0x5A)
+        xi.copy_(t.to(DEV))
+        xo, raw, a, b = _padded(t.numel(), tdt, offset, 0xA5)
+        ins.append(xi)
+        outs.append(xo)
+        raws.append((raw, a, b))
+    with basp.Layout(B, S, Hq, Hkv, d, N, K, dtype) as L:
+        ws = wraw = None
+        if algo == "three_pass":
+            ws, wraw, wa, wb = _padded(L.info["workspace_bytes"], torch.uint8,
+                                       offset, 0x3C)
+        basp.basp_seq2head(L.handle, algo, ins[0], ins[1], ins[2],
+                           outs[0], outs[1], outs[2], ws)
+        basp.basp_head2seq(L.handle, algo, ins[3], None, None, outs[3], None,
+                           None, ws)
+        torch.cuda.synchronize()
+    for name, g, e in zip("qkvo", outs, exp):
+        assert_bits_equal(g, e, "offset %d %s %s" % (offset, algo, name))
+    for raw, a, b in raws:
+        assert bool((raw[:a] == 0xA5).all()) and bool((raw[b:] == 0xA5).all())
+    if wraw is not None:
+        assert bool((wraw[:wa] == 0x3C).all()) and bool((wraw[wb:] == 0x3C).all())
+
+
+@pytest.mark.parametrize("which", ["q", "kv", "k"])
+def test_subsets_of_tensors(which):
+    B, S, Hq, Hkv, d, N, K = 2, 128, 16, 8, 32, 8, 4
+    q, k, v, o = make_inputs(B, S, Hq, Hkv, d, "bf16", 17, kind="bits")
+    exp = oracle_outputs(q, k, v, o, B, S, Hq, Hkv, d, N, K)
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    outs = [torch.zeros_like(t) for t in (qd, kd, vd)]
+    use = {"q": (1, 0, 0), "kv": (0, 1, 1), "k": (0, 1, 0)}[which]
+    args = [t if u else None for t, u in zip((qd, kd, vd), use)]
+    oargs = [t if u else None for t, u in zip(outs, use)]
+    with basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16") as L:
+        for algo in ALGOS:
+            ws = torch.empty(L.info["workspace_bytes"], dtype=torch.uint8, device=DEV)
+            for t in outs:
+                t.zero_()
+            basp.basp_seq2head(L.handle, algo, *args, *oargs, ws)
+            torch.cuda.synchronize()
+            for u, g, e, nm in zip(use, outs, exp[:3], "qkv"):
+                if u:
+                    assert_bits_equal(g, e, "%s %s %s" % (which, algo, nm))
+                else:
+                    assert int(g.view(torch.int16).abs().sum()) == 0
+
+
+def test_side_stream():
+    B, S, Hq, Hkv, d, N, K = 2, 1024, 32, 8, 64, 8, 4
+    q, k, v, o = make_inputs(B, S, Hq, Hkv, d, "bf16", 23)
+    exp = oracle_outputs(q, k, v, o, B, S, Hq, Hkv, d, N, K)
+    s = torch.cuda.Stream()
+    for algo in ALGOS:
+        got = device_outputs(q, k, v, o, B, S, Hq, Hkv, d, N, K, "bf16", algo,
+                             stream=s)
+        for name, g, e in zip("qkvo", got, exp):
+            assert_bits_equal(g, e, "side stream %s %s" % (algo, name))
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_host_buffer_entry_points(algo):
+    """basp_seq2head_host / basp_head2seq_host: pinned host in, pinned host
+    out, device staging owned by the caller."""
+    B, S, Hq, Hkv, d, N, K = 2, 2048, 32, 8, 64, 8, 4
+    q, k, v, o = make_inputs(B, S, Hq, Hkv, d, "bf16", 31)
+    exp = oracle_outputs(q, k, v, o, B, S, Hq, Hkv, d, N, K)
+    hin = [t.pin_memory() for t in (q, k, v, o)]
+    hout = [torch.empty_like(t).pin_memory() for t in hin]
+    with basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16") as L:
+        staging = torch.empty(L.info["staging_bytes"], dtype=torch.uint8, device=DEV)
+        ws = torch.empty(L.info["workspace_bytes"], dtype=torch.uint8, device=DEV)
+        st = torch.cuda.current_stream()
+        basp.basp_seq2head_host(L.handle, algo, hin[0], hin[1], hin[2],
+                                hout[0], hout[1], hout[2], staging,
+                                workspace=ws, stream=st)
+        basp.basp_head2seq_host(L.handle, algo, hin[3], None, None, hout[3],
+                                None, None, staging, workspace=ws, stream=st)
+        st.synchronize()
+    for name, g, e in zip("qkvo", hout, exp):
+        np.testing.assert_array_equal(synth_inputs.bits(g), e, err_msg=name)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_above_2_to_31_elements_sampled(algo):
+    """A Q buffer of 2^31 bf16 elements (4 GiB; byte offsets past 2^32):
+    round trip restores every bit, and 1<<14 sampled output elements match
+    the oracle's single-element map."""
+    B, S, H, d, N, K = 2, 262144, 32, 128, 8, 4
+    n = B * S * H * d
+    assert n == 1 << 31
+    x = synth_inputs.random_bits_device(n, 77, "bf16", DEV)
+    y = torch.empty_like(x)
+    with basp.Layout(B, S, H, 8, d, N, K, "bf16") as L:
+        ws = None
+        if algo == "three_pass":
+            ws = torch.empty(2 * L.info["bytes_q"] + 512, dtype=torch.uint8, device=DEV)
+        basp.basp_seq2head(L.handle, algo, x, None, None, y, None, None, ws)
+        torch.cuda.synchronize()
+        g = torch.Generator().manual_seed(5)
+        idx = torch.randint(0, n, (1 << 14,), generator=g)
+        src = torch.tensor([oracle.head_to_seq_index(B, S, H, d, N, K, int(i))
+                            for i in idx])
+        got = y.view(torch.int16)[idx.to(DEV)].cpu()
+        want = x.view(torch.int16)[src.to(DEV)].cpu()
+        assert torch.equal(got, want)
+        z = torch.empty_like(x)
+        basp.basp_head2seq(L.handle, algo, y, None, None, z, None, None, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(z.view(torch.int16), x.view(torch.int16))
+    del x, y, z, ws
+    torch.cuda.empty_cache()
