@@ -184,6 +184,44 @@ basp_status basp_head2seq_host(const basp_layout *layout, basp_algo algo,
                                void *workspace, size_t workspace_bytes,
                                cudaStream_t stream);
 
+/*
+ * basp_seq2head_noalloc -- seq-sharded -> head-sharded through the three-pass
+ * path (pack, exchange, unpack), with the scratch it needs taken from a buffer
+ * built into the library instead of from the caller.  The paper has no
+ * counterpart to this call; it exists for callers that cannot allocate device
+ * memory when they need the re-layout: code that runs inside a host
+ * framework's custom-op or plugin interface whose caching allocator owns all
+ * device memory and hands out no scratch, and latency-bound serving loops that
+ * ban cudaMalloc on their hot path because it can synchronise the device and
+ * take milliseconds.  Such callers still pass their own inputs and outputs.
+ *
+ * The scratch is one file-scope __device__ array of
+ * BASP_NOALLOC_SCRATCH_BYTES (32 MiB).  Every GPU on which the library's
+ * device code is loaded holds it until the process exits.  A call needs
+ * 2 * (bytes of each tensor it moves, each rounded up to 256) of it; a call
+ * that needs more returns BASP_ERR_WORKSPACE and launches nothing (use
+ * basp_seq2head with a workspace instead).  With Llama-3.2-1B heads
+ * (Hq=32, Hkv=8, d=64, bf16, B=2) Q, K and V together fit up to S=1024.
+ *
+ * The first call on each device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, with that device current), which may load the
+ * library's device code there; make that first call before any stream
+ * capture.  Every call shares the one array: calls whose kernels can overlap
+ * on the GPU (different streams, or several host threads) race on it and
+ * corrupt each other's results, so keep them on one stream.  Each call
+ * writes every scratch byte before reading it, so nothing has to start at
+ * zero and nothing is cleared between calls.  This call allocates nothing:
+ * no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * Arguments as for basp_seq2head with algo = BASP_ALGO_THREE_PASS and no
+ * workspace.
+ */
+#define BASP_NOALLOC_SCRATCH_BYTES (32u << 20)
+basp_status basp_seq2head_noalloc(const basp_layout *layout,
+                                  const void *q, const void *k, const void *v,
+                                  void *q_out, void *k_out, void *v_out,
+                                  cudaStream_t stream);
+
 /* Static English text for a status code. */
 const char *basp_status_string(basp_status status);
 

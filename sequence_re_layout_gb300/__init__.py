@@ -8,4 +8,5 @@ from .binding import (  # noqa: F401
     BASP_ERR_INVALID_ARG, BASP_ERR_TOO_LARGE, BASP_ERR_WORKSPACE, BASP_OK,
     DTYPE_CODES, EXPORTS, BaspError, Layout, basp_head2seq, basp_head2seq_host,
     basp_layout_create, basp_layout_destroy, basp_layout_query, basp_seq2head,
-    basp_seq2head_host, basp_status_string, load_library)
+    basp_seq2head_host, basp_seq2head_noalloc, basp_status_string,
+    BASP_NOALLOC_SCRATCH_BYTES, load_library)

@@ -27,7 +27,10 @@ ALGO_CODES = {"fused": BASP_ALGO_FUSED, "three_pass": BASP_ALGO_THREE_PASS}
 # every symbol include/basp.h declares
 EXPORTS = ("basp_layout_create", "basp_layout_query", "basp_layout_destroy",
            "basp_seq2head", "basp_head2seq", "basp_seq2head_host",
-           "basp_head2seq_host", "basp_status_string")
+           "basp_head2seq_host", "basp_seq2head_noalloc", "basp_status_string")
+
+# size of the library's built-in scratch for basp_seq2head_noalloc
+BASP_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class basp_info(ctypes.Structure):
@@ -76,6 +79,8 @@ def load_library():
         fn = getattr(lib, name)
         fn.argtypes = [vp, ctypes.c_int] + [vp] * 6 + [vp, sz, vp, sz, vp]
         fn.restype = ctypes.c_int
+    lib.basp_seq2head_noalloc.argtypes = [vp] + [vp] * 6 + [vp]
+    lib.basp_seq2head_noalloc.restype = ctypes.c_int
     lib.basp_status_string.argtypes = [ctypes.c_int]
     lib.basp_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -184,6 +189,16 @@ def basp_head2seq_host(layout, algo, o, k, v, o_out, k_out, v_out, staging,
         layout, _algo(algo), _ptr(o), _ptr(k), _ptr(v), _ptr(o_out),
         _ptr(k_out), _ptr(v_out), _ptr(staging), sb, _ptr(workspace), wb,
         _stream(stream)), "basp_head2seq_host")
+
+
+def basp_seq2head_noalloc(layout, q, k, v, q_out, k_out, v_out, stream=None):
+    """seq-sharded -> head-sharded through the three-pass path, using the
+    library's built-in scratch instead of a workspace: for callers that cannot
+    allocate device memory.  See ``basp.h`` for the size limit and the rule
+    that calls sharing the scratch must not overlap on the GPU."""
+    _check(load_library().basp_seq2head_noalloc(
+        layout, _ptr(q), _ptr(k), _ptr(v), _ptr(q_out), _ptr(k_out),
+        _ptr(v_out), _stream(stream)), "basp_seq2head_noalloc")
 
 
 class Layout:

@@ -42,6 +42,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "layout_internal.h"
 
@@ -582,4 +583,59 @@ extern "C" basp_status basp_head2seq_host(const basp_layout *L, basp_algo algo,
                                           void *ws, size_t ws_bytes, cudaStream_t stream) {
     return relayout_host(L, algo, false, o, k, v, o_out, k_out, v_out, staging,
                          staging_bytes, ws, ws_bytes, stream);
+}
+
+// ---------------------------------------------------------------------------
+// basp_seq2head_noalloc: the three-pass seq2head with its scratch in a static
+// device array, for callers that cannot allocate (see basp.h).
+// ---------------------------------------------------------------------------
+
+static __device__ __align__(256) unsigned char
+    g_noalloc_scratch[BASP_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_setup_mutex;
+std::atomic<void *> g_noalloc_addr[kMaxDevices];
+
+// The array's device address on the current device.  In host code the name
+// g_noalloc_scratch is only a host-side stand-in, so the address is looked up
+// once per device, with that device current.
+basp_status noalloc_scratch(void **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BASP_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return BASP_ERR_INVALID_ARG;
+    void *p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        std::lock_guard<std::mutex> lock(g_noalloc_setup_mutex);
+        p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+        if (p == nullptr) {
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess ||
+                p == nullptr)
+                return BASP_ERR_CUDA;
+            g_noalloc_addr[dev].store(p, std::memory_order_release);
+        }
+    }
+    *out = p;
+    return BASP_OK;
+}
+
+}  // namespace
+
+extern "C" basp_status basp_seq2head_noalloc(const basp_layout *L,
+                                             const void *q, const void *k, const void *v,
+                                             void *q_out, void *k_out, void *v_out,
+                                             cudaStream_t stream) {
+    TensorArg t[3];
+    int n = 0;
+    basp_status st = collect(L, q, k, v, q_out, k_out, v_out, t, &n);
+    if (st != BASP_OK) return st;
+    if (region_bytes(*L, t, n) > int64_t(BASP_NOALLOC_SCRATCH_BYTES))
+        return BASP_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != BASP_OK) return st;
+    return relayout(L, BASP_ALGO_THREE_PASS, true, q, k, v, q_out, k_out, v_out,
+                    scratch, size_t(BASP_NOALLOC_SCRATCH_BYTES), stream);
 }

@@ -153,6 +153,11 @@ def test_compute_rejects_before_launch(layout):
         (lambda: basp.basp_seq2head_host(h, "fused", FAKE, None, None, FAKE + nq, None, None,
                                          None, 0),
          basp.BASP_ERR_WORKSPACE),
+        # no-allocation form: unpaired, aliasing
+        (lambda: basp.basp_seq2head_noalloc(h, FAKE, None, None, None, None, None),
+         basp.BASP_ERR_INVALID_ARG),
+        (lambda: basp.basp_seq2head_noalloc(h, FAKE, None, None, FAKE + 2, None, None),
+         basp.BASP_ERR_ALIASING),
     ]
     for fn, status in cases:
         with pytest.raises(basp.BaspError) as e:
@@ -164,3 +169,13 @@ def test_status_strings():
     for s in range(9):
         assert basp.basp_status_string(s) not in ("", "unknown status")
     assert basp.basp_status_string(99) == "unknown status"
+
+
+def test_noalloc_size_limit_checked_before_any_cuda_call():
+    """A call needing more scratch than the built-in buffer is refused on the
+    host (this CPU-only run has no CUDA device to fall back on)."""
+    with basp.Layout(2, 4096, 32, 8, 64, 8, 4, "bf16") as L:
+        nq = L.info["bytes_q"]
+        with pytest.raises(basp.BaspError) as e:
+            basp.basp_seq2head_noalloc(L.handle, FAKE, None, None, FAKE + nq, None, None)
+        assert e.value.status == basp.BASP_ERR_WORKSPACE

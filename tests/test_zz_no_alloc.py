@@ -1,0 +1,58 @@
+"""basp_seq2head_noalloc: the three-pass seq->head re-layout with the
+library's built-in scratch, for callers that cannot allocate device memory
+(a host framework's plugin interface whose allocator owns all device memory,
+a serving loop that bans cudaMalloc on its hot path).
+
+Two calls in a row through the C ABI, each on fresh inputs, must give the same
+bits as the ordinary entry point basp_seq2head (and hence the oracle); a call
+whose scratch would exceed the built-in buffer is refused before any launch.
+This file is collected last on purpose: it shares no state with the others
+and passes alone or after them.
+"""
+import pytest
+import torch
+
+import synth_inputs
+import sequence_re_layout_gb300 as basp
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.mark.parametrize("shape", [
+    # (B, S, Hq, Hkv, d, N, K): Llama-3.2-1B heads at S=1024 (24 MiB of
+    # scratch for Q, K, V), BASP and Ulysses
+    (2, 1024, 32, 8, 64, 8, 4),
+    (2, 1024, 32, 8, 64, 8, 8),
+])
+def test_noalloc_matches_seq2head_on_two_calls(shape):
+    B, S, Hq, Hkv, d, N, K = shape
+    nq, nkv = B * S * Hq * d, B * S * Hkv * d
+    with basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16") as L:
+        assert 2 * (L.info["bytes_q"] + 2 * L.info["bytes_kv"]) <= basp.BASP_NOALLOC_SCRATCH_BYTES
+        for call, seed in enumerate((101, 202)):
+            ins = [synth_inputs.random_bits(n, seed + i, "bf16").to(DEV)
+                   for i, n in enumerate((nq, nkv, nkv))]
+            want = [torch.empty_like(t) for t in ins]
+            got = [torch.full_like(t, float("nan")) for t in ins]
+            basp.basp_seq2head(L.handle, "fused", *ins, *want)
+            basp.basp_seq2head_noalloc(L.handle, *ins, *got)
+            torch.cuda.synchronize()
+            for name, g, w in zip("qkv", got, want):
+                assert torch.equal(g.view(torch.int16), w.view(torch.int16)), \
+                    "call %d tensor %s differs" % (call, name)
+
+
+def test_noalloc_refuses_more_than_its_scratch():
+    # S=2048: Q, K and V need 48 MiB of scratch, more than the 32 MiB built in
+    B, S, Hq, Hkv, d, N, K = 2, 2048, 32, 8, 64, 8, 4
+    with basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16") as L:
+        ins = [torch.zeros(B * S * h * d, dtype=torch.bfloat16, device=DEV)
+               for h in (Hq, Hkv, Hkv)]
+        outs = [torch.zeros_like(t) for t in ins]
+        with pytest.raises(basp.BaspError) as e:
+            basp.basp_seq2head_noalloc(L.handle, *ins, *outs)
+        assert e.value.status == basp.BASP_ERR_WORKSPACE
+        # Q alone (16 MiB of scratch) fits
+        basp.basp_seq2head_noalloc(L.handle, ins[0], None, None, outs[0], None, None)
+        torch.cuda.synchronize()
