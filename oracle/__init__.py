@@ -31,6 +31,18 @@ fugumt.com related-papers entry "DeepSpeed Ulysses"):
 
 The elements are opaque words: pass any numpy dtype (bf16 travels as uint16).
 The result is a bit copy, so tests compare raw bits.
+
+Two variants, neither fixed by the pages (which give no memory order and no
+projection layout):
+
+* ``order="sbhd"``: sequence-first shards, the [S, B, H, d] activation order
+  of Megatron-style stacks: seq-sharded ``[S/K, Bg, H, d]``, head-sharded
+  ``[S, Bg, H/K, d]``.
+* packed QKV: the seq-sharded input is one buffer whose every token row holds
+  the Hq query heads, then the Hkv key heads, then the Hkv value heads (the
+  output of a fused QKV projection).  ``seq2head_qkv`` splits each token row
+  into those three head ranges and re-lays each out; ``head2seq_qkv`` is the
+  inverse.
 """
 from __future__ import annotations
 
@@ -66,6 +78,10 @@ def _load():
             fn = getattr(lib, name)
             fn.argtypes = [i64] * 7 + [ctypes.c_void_p, ctypes.c_void_p]
             fn.restype = ctypes.c_int
+        for name in ("basp_oracle_seq2head_ordered", "basp_oracle_head2seq_ordered"):
+            fn = getattr(lib, name)
+            fn.argtypes = [i64] * 7 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+            fn.restype = ctypes.c_int
         fn = lib.basp_oracle_head_to_seq_index
         fn.argtypes = [i64] * 7
         fn.restype = i64
@@ -90,7 +106,10 @@ def valid_shape(B, S, H, d, N, K) -> bool:
     return True
 
 
-def _run(fn_name, x, B, S, H, d, N, K):
+ORDERS = {"bshd": 0, "sbhd": 1}
+
+
+def _run(fn_name, x, B, S, H, d, N, K, order="bshd"):
     x = np.ascontiguousarray(x)
     n = B * S * H * d
     if x.size != n:
@@ -98,22 +117,58 @@ def _run(fn_name, x, B, S, H, d, N, K):
     out = np.empty_like(x)
     if n == 0:
         return out
-    rc = getattr(_load(), fn_name)(B, S, H, d, N, K, x.itemsize,
-                                   x.ctypes.data, out.ctypes.data)
+    if order == "bshd":
+        rc = getattr(_load(), fn_name)(B, S, H, d, N, K, x.itemsize,
+                                       x.ctypes.data, out.ctypes.data)
+    else:
+        rc = getattr(_load(), fn_name + "_ordered")(
+            B, S, H, d, N, K, x.itemsize, ORDERS[order], x.ctypes.data,
+            out.ctypes.data)
     if rc != 0:
         raise ValueError("shape breaks a divisibility rule")
     return out
 
 
-def seq2head(x, B, S, H, d, N, K):
+def seq2head(x, B, S, H, d, N, K, order="bshd"):
     """seq-sharded buffer (N shards of [Bg, S/K, H, d]) -> head-sharded buffer
-    (N shards of [Bg, S, H/K, d]).  Plain C element loop."""
-    return _run("basp_oracle_seq2head", x, B, S, H, d, N, K)
+    (N shards of [Bg, S, H/K, d]).  Plain C element loop.  ``order="sbhd"``
+    takes sequence-first shards ([S/K, Bg, H, d] -> [S, Bg, H/K, d])."""
+    return _run("basp_oracle_seq2head", x, B, S, H, d, N, K, order)
 
 
-def head2seq(x, B, S, H, d, N, K):
+def head2seq(x, B, S, H, d, N, K, order="bshd"):
     """Inverse of :func:`seq2head`.  Plain C element loop."""
-    return _run("basp_oracle_head2seq", x, B, S, H, d, N, K)
+    return _run("basp_oracle_head2seq", x, B, S, H, d, N, K, order)
+
+
+def split_packed_qkv(x, Hq, Hkv, d):
+    """Cut a packed QKV buffer (token rows of Hq + 2*Hkv heads) into the
+    Q, K and V buffers with the same token rows."""
+    rows = x.reshape(-1, Hq + 2 * Hkv, d)
+    return (np.ascontiguousarray(rows[:, :Hq]).reshape(-1),
+            np.ascontiguousarray(rows[:, Hq:Hq + Hkv]).reshape(-1),
+            np.ascontiguousarray(rows[:, Hq + Hkv:]).reshape(-1))
+
+
+def join_packed_qkv(q, k, v, Hq, Hkv, d):
+    """Inverse of :func:`split_packed_qkv`."""
+    return np.concatenate([q.reshape(-1, Hq, d), k.reshape(-1, Hkv, d),
+                           v.reshape(-1, Hkv, d)], axis=1).reshape(-1)
+
+
+def seq2head_qkv(x, B, S, Hq, Hkv, d, N, K, order="bshd"):
+    """Packed seq-sharded QKV -> head-sharded Q, K, V (three buffers)."""
+    q, k, v = split_packed_qkv(x, Hq, Hkv, d)
+    return (seq2head(q, B, S, Hq, d, N, K, order),
+            seq2head(k, B, S, Hkv, d, N, K, order),
+            seq2head(v, B, S, Hkv, d, N, K, order))
+
+
+def head2seq_qkv(q, k, v, B, S, Hq, Hkv, d, N, K, order="bshd"):
+    """Head-sharded Q, K, V -> one packed seq-sharded buffer."""
+    return join_packed_qkv(head2seq(q, B, S, Hq, d, N, K, order),
+                           head2seq(k, B, S, Hkv, d, N, K, order),
+                           head2seq(v, B, S, Hkv, d, N, K, order), Hq, Hkv, d)
 
 
 def head_to_seq_index(B, S, H, d, N, K, o):
@@ -179,13 +234,69 @@ def unshard_head(x, B, S, H, d, N, K):
     return X
 
 
-def seq2head_by_slices(x, B, S, H, d, N, K):
+def shard_seq_sf(X, N, K):
+    """Cut X[S, B, H, d] (sequence-first logical tensor) into the
+    sequence-first seq-sharded buffer: shard (g, j) = X[j-th token block,
+    group g's sequences], stored [S/K, Bg, H, d]."""
+    S, B, H, d = X.shape
+    G, Bg = groups(N, K, B)
+    Sk = S // K
+    parts = []
+    for r in range(N):
+        g, j = divmod(r, K)
+        parts.append(X[j * Sk:(j + 1) * Sk, g * Bg:(g + 1) * Bg].reshape(-1))
+    return np.concatenate(parts) if parts else X.reshape(-1)
+
+
+def shard_head_sf(X, N, K):
+    """Cut X[S, B, H, d] into the sequence-first head-sharded buffer: shard
+    (g, j') = X[all tokens, group g's sequences, j'-th head block], stored
+    [S, Bg, H/K, d]."""
+    S, B, H, d = X.shape
+    G, Bg = groups(N, K, B)
+    Hk = H // K
+    parts = []
+    for r in range(N):
+        g, jp = divmod(r, K)
+        parts.append(X[:, g * Bg:(g + 1) * Bg, jp * Hk:(jp + 1) * Hk].reshape(-1))
+    return np.concatenate(parts) if parts else X.reshape(-1)
+
+
+def unshard_seq_sf(x, B, S, H, d, N, K):
+    G, Bg = groups(N, K, B)
+    Sk = S // K
+    X = np.empty((S, B, H, d), dtype=x.dtype)
+    P = Sk * Bg * H * d
+    for r in range(N):
+        g, j = divmod(r, K)
+        X[j * Sk:(j + 1) * Sk, g * Bg:(g + 1) * Bg] = \
+            x[r * P:(r + 1) * P].reshape(Sk, Bg, H, d)
+    return X
+
+
+def unshard_head_sf(x, B, S, H, d, N, K):
+    G, Bg = groups(N, K, B)
+    Hk = H // K
+    X = np.empty((S, B, H, d), dtype=x.dtype)
+    P = S * Bg * Hk * d
+    for r in range(N):
+        g, jp = divmod(r, K)
+        X[:, g * Bg:(g + 1) * Bg, jp * Hk:(jp + 1) * Hk] = \
+            x[r * P:(r + 1) * P].reshape(S, Bg, Hk, d)
+    return X
+
+
+def seq2head_by_slices(x, B, S, H, d, N, K, order="bshd"):
     if not valid_shape(B, S, H, d, N, K):
         raise ValueError("shape breaks a divisibility rule")
+    if order == "sbhd":
+        return shard_head_sf(unshard_seq_sf(x, B, S, H, d, N, K), N, K)
     return shard_head(unshard_seq(x, B, S, H, d, N, K), N, K)
 
 
-def head2seq_by_slices(x, B, S, H, d, N, K):
+def head2seq_by_slices(x, B, S, H, d, N, K, order="bshd"):
     if not valid_shape(B, S, H, d, N, K):
         raise ValueError("shape breaks a divisibility rule")
+    if order == "sbhd":
+        return shard_seq_sf(unshard_head_sf(x, B, S, H, d, N, K), N, K)
     return shard_seq(unshard_head(x, B, S, H, d, N, K), N, K)

@@ -35,7 +35,9 @@
  *   `esz`-byte words, so the result is a pure bit copy (no rounding).
  *
  * Readings where the pages are silent (each listed in the design notes):
- *   - batch-first [B, S, H, d] order inside a shard;
+ *   - batch-first [B, S, H, d] order inside a shard (the *_ordered entry
+ *     points also take the sequence-first [S, B, H, d] order of Megatron-style
+ *     stacks: shards [S/K][Bg][H][d] and [S][Bg][H/K][d]);
  *   - member j of a group holds the j-th contiguous block of S/K tokens;
  *   - member j' receives the j'-th contiguous block of H/K heads.
  *
@@ -63,10 +65,24 @@ static int shape_ok(int64_t B, int64_t S, int64_t H, int64_t d, int64_t N,
  * dir = 0: seq2head (read seq-sharded `a`, write head-sharded `b`).
  * dir = 1: head2seq (read head-sharded `b`, write seq-sharded `a`).
  * `a` and `b` are byte pointers; offsets below are in elements.
+ * order = 0: batch-first shards ([Bg][S/K][H][d] and [Bg][S][H/K][d]);
+ * order = 1: sequence-first shards ([S/K][Bg][H][d] and [S][Bg][H/K][d]), the
+ *            [S, B, H, d] activation order of Megatron-style stacks.
  */
+static int walk_ordered(int64_t B, int64_t S, int64_t H, int64_t d, int64_t N,
+                        int64_t K, int64_t esz, unsigned char *a,
+                        unsigned char *b, int dir, int order);
+
 static int walk(int64_t B, int64_t S, int64_t H, int64_t d, int64_t N,
                 int64_t K, int64_t esz, unsigned char *a, unsigned char *b,
                 int dir)
+{
+    return walk_ordered(B, S, H, d, N, K, esz, a, b, dir, 0);
+}
+
+static int walk_ordered(int64_t B, int64_t S, int64_t H, int64_t d, int64_t N,
+                        int64_t K, int64_t esz, unsigned char *a,
+                        unsigned char *b, int dir, int order)
 {
     if (!shape_ok(B, S, H, d, N, K, esz)) return -1;
     const int64_t G  = N / K;        /* groups                      */
@@ -85,9 +101,12 @@ static int walk(int64_t B, int64_t S, int64_t H, int64_t d, int64_t N,
                     const int64_t jp = h / Hk;           /* member that gets head h */
                     const int64_t hl = h % Hk;
                     const int64_t r_out = g * K + jp;
+                    /* token position inside each shard, by order */
+                    const int64_t t_in  = order ? sl * Bg + bl : bl * Sk + sl;
+                    const int64_t t_out = order ? s * Bg + bl  : bl * S + s;
                     for (int64_t e = 0; e < d; ++e) {
-                        const int64_t src = r_in * P + ((bl * Sk + sl) * H + h) * d + e;
-                        const int64_t dst = r_out * P + ((bl * S + s) * Hk + hl) * d + e;
+                        const int64_t src = r_in * P + (t_in * H + h) * d + e;
+                        const int64_t dst = r_out * P + (t_out * Hk + hl) * d + e;
                         if (dir == 0)
                             memcpy(b + dst * esz, a + src * esz, (size_t)esz);
                         else
@@ -98,6 +117,24 @@ static int walk(int64_t B, int64_t S, int64_t H, int64_t d, int64_t N,
         }
     }
     return 0;
+}
+
+int basp_oracle_seq2head_ordered(int64_t B, int64_t S, int64_t H, int64_t d,
+                                 int64_t N, int64_t K, int64_t esz, int order,
+                                 const void *in, void *out)
+{
+    if (order != 0 && order != 1) return -1;
+    return walk_ordered(B, S, H, d, N, K, esz, (unsigned char *)in,
+                        (unsigned char *)out, 0, order);
+}
+
+int basp_oracle_head2seq_ordered(int64_t B, int64_t S, int64_t H, int64_t d,
+                                 int64_t N, int64_t K, int64_t esz, int order,
+                                 const void *in, void *out)
+{
+    if (order != 0 && order != 1) return -1;
+    return walk_ordered(B, S, H, d, N, K, esz, (unsigned char *)out,
+                        (unsigned char *)in, 1, order);
 }
 
 int basp_oracle_seq2head(int64_t B, int64_t S, int64_t H, int64_t d,

@@ -31,23 +31,42 @@ def _read_golden():
             if not line:
                 continue
             tok = line.split()
-            if tok[0] == "case":
+            if tok[0] in ("case", "qkvcase"):
                 kv = dict(t.split("=") for t in tok[2:])
-                cur = {"name": tok[1], **{k: int(v) for k, v in kv.items()}}
+                cur = {"kind": tok[0], "name": tok[1], "order": kv.pop("order", "bshd"),
+                       **{k: int(v) for k, v in kv.items()}}
                 cases.append(cur)
             else:
                 cur[tok[0]] = np.array([float(t) for t in tok[1:]], np.float32)
     return cases
 
 
-@pytest.mark.parametrize("case", _read_golden(), ids=lambda c: c["name"])
+GOLDEN_CASES = _read_golden()
+
+
+@pytest.mark.parametrize("case", [c for c in GOLDEN_CASES if c["kind"] == "case"],
+                         ids=lambda c: c["name"])
 def test_hand_worked_values(case):
     c = case
     args = (c["B"], c["S"], c["H"], c["d"], c["N"], c["K"])
-    np.testing.assert_array_equal(oracle.seq2head(c["seq"], *args), c["head"])
-    np.testing.assert_array_equal(oracle.head2seq(c["head"], *args), c["seq"])
-    np.testing.assert_array_equal(oracle.seq2head_by_slices(c["seq"], *args), c["head"])
-    np.testing.assert_array_equal(oracle.head2seq_by_slices(c["head"], *args), c["seq"])
+    o = c["order"]
+    np.testing.assert_array_equal(oracle.seq2head(c["seq"], *args, order=o), c["head"])
+    np.testing.assert_array_equal(oracle.head2seq(c["head"], *args, order=o), c["seq"])
+    np.testing.assert_array_equal(oracle.seq2head_by_slices(c["seq"], *args, order=o), c["head"])
+    np.testing.assert_array_equal(oracle.head2seq_by_slices(c["head"], *args, order=o), c["seq"])
+
+
+@pytest.mark.parametrize("case", [c for c in GOLDEN_CASES if c["kind"] == "qkvcase"],
+                         ids=lambda c: c["name"])
+def test_hand_worked_packed_qkv(case):
+    c = case
+    args = (c["B"], c["S"], c["Hq"], c["Hkv"], c["d"], c["N"], c["K"])
+    q, k, v = oracle.seq2head_qkv(c["packed"], *args)
+    np.testing.assert_array_equal(q, c["q"])
+    np.testing.assert_array_equal(k, c["k"])
+    np.testing.assert_array_equal(v, c["v"])
+    np.testing.assert_array_equal(oracle.head2seq_qkv(c["q"], c["k"], c["v"], *args),
+                                  c["packed"])
 
 
 def tiny_shapes():
