@@ -48,6 +48,10 @@ def parse_args():
     p.add_argument("--layout", default="basp", choices=["basp", "ulysses"])
     p.add_argument("--algo", default="fused", choices=["fused", "three_pass"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--order", default="bshd", choices=["bshd", "sbhd"],
+                   help="token order inside the shards (batch- or sequence-first)")
+    p.add_argument("--qkv-packed", action="store_true",
+                   help="seq2head reads one packed QKV projection output")
     p.add_argument("--soak-s", type=float, default=1.0,
                    help="untimed seconds at full load before the timed region "
                         "(so the clock samples see the loaded GPU)")
@@ -211,33 +215,38 @@ def ncu_traffic(workload: str, layout: str, kernel_role: str):
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def _alloc_sets(w, K, dtype, n_sets, dev, seed):
+def _alloc_sets(w, K, dtype, n_sets, dev, seed, packed=False):
     import torch
     import synth_inputs
     nq, nkv = w.tensor_elems(w.Hq), w.tensor_elems(w.Hkv)
     base = [synth_inputs.normal(n, seed + i, dtype).to(dev)
             for i, n in enumerate((nq, nkv, nkv, nq))]
+    if packed:
+        # ins[0] is the packed QKV buffer; ins[1], ins[2] are unused
+        base[0] = synth_inputs.normal(nq + 2 * nkv, seed + 7, dtype).to(dev)
     sets = []
     for s in range(n_sets):
         ins = base if s == 0 else [t.clone() for t in base]
-        outs = [torch.empty_like(t) for t in ins]
+        outs = [torch.empty(n, dtype=ins[3].dtype, device=dev)
+                for n in (nq, nkv, nkv, nq)]
         sets.append((ins, outs))
     return sets
 
 
-def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, sampler_cb=None):
+def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
+               packed=False):
     """Time `steps` steps of the hot path; returns a dict of timings."""
     import torch
     import sequence_re_layout_gb300 as basp
 
     K = w.K(layout)
-    L = basp.Layout(w.B, w.S, w.Hq, w.Hkv, w.d, w.N, K, w.dtype)
+    L = basp.Layout(w.B, w.S, w.Hq, w.Hkv, w.d, w.N, K, w.dtype, order=order)
     info = L.info
     T = info["bytes_q"] * 2 + info["bytes_kv"] * 2            # Q, K, V, O
     step_bytes = 2 * T
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     n_sets = min(4096, max(2, -(-4 * l2 // step_bytes) + 1))   # >= 4x L2 per rotation
-    sets = _alloc_sets(w, K, w.dtype, n_sets, dev, 1234)
+    sets = _alloc_sets(w, K, w.dtype, n_sets, dev, 1234, packed)
     ws = None
     if algo == "three_pass":
         ws = torch.empty(info["workspace_bytes"], dtype=torch.uint8, device=dev)
@@ -247,8 +256,12 @@ def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, sampler_cb=None)
         ins, outs = sets[i % n_sets]
         if ev is not None:
             ev[0].record(stream)
-        basp.basp_seq2head(L.handle, algo, ins[0], ins[1], ins[2],
-                           outs[0], outs[1], outs[2], ws, stream=stream)
+        if packed:
+            basp.basp_seq2head_qkv(L.handle, ins[0], outs[0], outs[1], outs[2],
+                                   stream=stream)
+        else:
+            basp.basp_seq2head(L.handle, algo, ins[0], ins[1], ins[2],
+                               outs[0], outs[1], outs[2], ws, stream=stream)
         if ev is not None:
             ev[1].record(stream)
         basp.basp_head2seq(L.handle, algo, ins[3], None, None,
@@ -390,8 +403,10 @@ def main_ours(args, dist):
 
     sampler = ClockSampler(dev.index)
     dist.barrier()
+    if args.qkv_packed and args.algo != "fused":
+        raise SystemExit("--qkv-packed runs the fused path only")
     r = run_device(w, args.layout, args.algo, args.steps, args.warmup, dev,
-                   soak_s=args.soak_s)
+                   soak_s=args.soak_s, order=args.order, packed=args.qkv_packed)
     sampler.stop()
     dist.barrier()
     t_max = dist.max(r["total_ms"])
@@ -401,7 +416,9 @@ def main_ours(args, dist):
 
     info = r["info"]
     s2h_gbs = gbs(r["s2h_bytes"], r["s2h_ms_mean"])
-    traffic = ncu_traffic(w.name, args.layout, "seq2head_qkv_" + args.algo)
+    traffic = None
+    if args.order == "bshd" and not args.qkv_packed:
+        traffic = ncu_traffic(w.name, args.layout, "seq2head_qkv_" + args.algo)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
@@ -410,6 +427,7 @@ def main_ours(args, dist):
         "data": "synthetic (~N(0,1) %s, seeded)" % w.dtype,
         "config": {
             "workload": w.name, "layout": args.layout, "algo": args.algo,
+            "order": args.order, "qkv_packed": bool(args.qkv_packed),
             "B": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "N": w.N,
             "K": info["K"], "groups": info["groups"],
             "bytes_per_step": r["step_bytes"],
@@ -440,7 +458,8 @@ def main_ours(args, dist):
     }
     if not args.no_extras and dist.rank == 0:
         other = "ulysses" if args.layout == "basp" else "basp"
-        ru = run_device(w, other, args.algo, args.steps, args.warmup, dev)
+        ru = run_device(w, other, args.algo, args.steps, args.warmup, dev,
+                        order=args.order, packed=args.qkv_packed)
         vu = gbs(ru["step_bytes"] * args.steps, ru["total_ms"])
         ou = ru["info"]
         out[other] = {"value": round(vu, 2), "ms_per_step": round(ru["ms_per_step"], 6),
@@ -449,7 +468,8 @@ def main_ours(args, dist):
                       "bytes_per_peer_q": ou["bytes_per_peer_q"],
                       "seq2head_gbs": round(gbs(ru["s2h_bytes"], ru["s2h_ms_mean"]), 2)}
         alt = "three_pass" if args.algo == "fused" else "fused"
-        rt = run_device(w, args.layout, alt, args.steps, args.warmup, dev)
+        rt = run_device(w, args.layout, alt, args.steps, args.warmup, dev,
+                        order=args.order)
         vt = gbs(rt["step_bytes"] * args.steps, rt["total_ms"])
         out[alt] = {"value": round(vt, 2), "ms_per_step": round(rt["ms_per_step"], 6),
                     "pct_hbm_peak": round(100 * vt / peak, 2),

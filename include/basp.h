@@ -58,6 +58,16 @@ typedef enum basp_dtype {
     BASP_DTYPE_FP16 = 2
 } basp_dtype;
 
+/* Token order inside every rank shard.  The pages fix none; batch-first is the
+ * default.  Sequence-first is the [S, B, H, d] activation order of
+ * Megatron-style stacks: seq-sharded shards [S/K][Bg][H][d], head-sharded
+ * shards [S][Bg][H/K][d].  With one sequence per group (every BASP layout) the
+ * two orders store the same bytes. */
+typedef enum basp_order {
+    BASP_ORDER_BSHD = 0,
+    BASP_ORDER_SBHD = 1
+} basp_order;
+
 typedef enum basp_algo {
     /* One pass: every element goes straight from its source place to its
      * destination place; Q, K and V (or O, K, V) in one kernel launch. */
@@ -102,7 +112,16 @@ typedef struct basp_info {
                                      held all B sequences (the "Ulysses with
                                      SP = N/B" alternative of the review's
                                      "Strengths" section, B*B*S/N at K = N/B) */
+    int64_t order;                /* basp_order of the shards                  */
+    int64_t bytes_qkv_packed;     /* packed QKV buffer: B*S*(Hq+2*Hkv)*d*esz   */
 } basp_info;
+
+/* Everything basp_layout_create takes, plus the token order. */
+typedef struct basp_layout_desc {
+    int64_t B, S, Hq, Hkv, d, N, K;
+    basp_dtype dtype;
+    basp_order order;
+} basp_layout_desc;
 
 /*
  * Create a layout handle.
@@ -125,6 +144,12 @@ typedef struct basp_info {
 basp_status basp_layout_create(int64_t B, int64_t S, int64_t Hq, int64_t Hkv,
                                int64_t d, int64_t N, int64_t K,
                                basp_dtype dtype, basp_layout **out);
+
+/* As basp_layout_create, with the token order of the shards (desc->order);
+ * basp_layout_create is this call with BASP_ORDER_BSHD.  BASP_ERR_INVALID_ARG
+ * for a NULL desc or an unknown order.  Host only. */
+basp_status basp_layout_create_ex(const basp_layout_desc *desc,
+                                  basp_layout **out);
 
 /* Fill *out with the derived sizes of a layout.  Host only. */
 basp_status basp_layout_query(const basp_layout *layout, basp_info *out);
@@ -161,6 +186,28 @@ basp_status basp_head2seq(const basp_layout *layout, basp_algo algo,
                           void *o_out, void *k_out, void *v_out,
                           void *workspace, size_t workspace_bytes,
                           cudaStream_t stream);
+
+/*
+ * Packed QKV forms (fused path, one launch).  A fused QKV projection writes one
+ * activation whose every token row holds the Hq query heads, then the Hkv key
+ * heads, then the Hkv value heads; its seq-sharded virtual-rank buffer has
+ * shards [Bg][S/K][Hq+2*Hkv][d] (or [S/K][Bg][Hq+2*Hkv][d] for
+ * BASP_ORDER_SBHD), info.bytes_qkv_packed bytes in all.
+ *   basp_seq2head_qkv   packed seq-sharded `qkv` -> head-sharded q_out (Hq
+ *                       heads), k_out, v_out (Hkv heads), the same buffers
+ *                       basp_seq2head produces; no split copy first.
+ *   basp_head2seq_qkv   the inverse: head-sharded q, k, v (in the backward
+ *                       pass, the gradients dQ, dK, dV) -> one packed
+ *                       seq-sharded buffer `qkv_out`.
+ * All four pointers are required.  The pages describe no projection layout;
+ * the head order inside the row is the plainest concatenation.
+ */
+basp_status basp_seq2head_qkv(const basp_layout *layout, const void *qkv,
+                              void *q_out, void *k_out, void *v_out,
+                              cudaStream_t stream);
+basp_status basp_head2seq_qkv(const basp_layout *layout, const void *q,
+                              const void *k, const void *v, void *qkv_out,
+                              cudaStream_t stream);
 
 /*
  * End-to-end forms for callers whose tensors live in host memory: enqueue on

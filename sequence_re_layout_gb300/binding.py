@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(PKG, "libbasp.so")
 # enums of basp.h
 BASP_DTYPE_BF16, BASP_DTYPE_FP32, BASP_DTYPE_FP16 = 0, 1, 2
 BASP_ALGO_FUSED, BASP_ALGO_THREE_PASS = 0, 1
+BASP_ORDER_BSHD, BASP_ORDER_SBHD = 0, 1
 (BASP_OK, BASP_ERR_INVALID_ARG, BASP_ERR_DIVISIBILITY, BASP_ERR_BATCH_GT_RANKS,
  BASP_ERR_ALIGNMENT, BASP_ERR_ALIASING, BASP_ERR_WORKSPACE, BASP_ERR_CUDA,
  BASP_ERR_TOO_LARGE) = range(9)
@@ -23,10 +24,12 @@ BASP_ALGO_FUSED, BASP_ALGO_THREE_PASS = 0, 1
 DTYPE_CODES = {"bf16": BASP_DTYPE_BF16, "fp32": BASP_DTYPE_FP32,
                "fp16": BASP_DTYPE_FP16}
 ALGO_CODES = {"fused": BASP_ALGO_FUSED, "three_pass": BASP_ALGO_THREE_PASS}
+ORDER_CODES = {"bshd": BASP_ORDER_BSHD, "sbhd": BASP_ORDER_SBHD}
 
 # every symbol include/basp.h declares
-EXPORTS = ("basp_layout_create", "basp_layout_query", "basp_layout_destroy",
-           "basp_seq2head", "basp_head2seq", "basp_seq2head_host",
+EXPORTS = ("basp_layout_create", "basp_layout_create_ex", "basp_layout_query",
+           "basp_layout_destroy", "basp_seq2head", "basp_head2seq",
+           "basp_seq2head_qkv", "basp_head2seq_qkv", "basp_seq2head_host",
            "basp_head2seq_host", "basp_seq2head_noalloc", "basp_status_string")
 
 # size of the library's built-in scratch for basp_seq2head_noalloc
@@ -38,10 +41,16 @@ class basp_info(ctypes.Structure):
         "B", "S", "Hq", "Hkv", "d", "N", "K", "groups", "seqs_per_group",
         "tokens_per_rank", "elem_size", "elems_per_rank_q", "elems_per_rank_kv",
         "peers", "bytes_per_peer_q", "bytes_per_peer_kv", "bytes_q", "bytes_kv",
-        "workspace_bytes", "staging_bytes", "foil_tokens_per_rank")]
+        "workspace_bytes", "staging_bytes", "foil_tokens_per_rank", "order",
+        "bytes_qkv_packed")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class basp_layout_desc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("B", "S", "Hq", "Hkv", "d", "N", "K")] + \
+        [("dtype", ctypes.c_int), ("order", ctypes.c_int)]
 
 
 class BaspError(RuntimeError):
@@ -67,6 +76,9 @@ def load_library():
     vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
     lib.basp_layout_create.argtypes = [i64] * 7 + [ctypes.c_int, ctypes.POINTER(vp)]
     lib.basp_layout_create.restype = ctypes.c_int
+    lib.basp_layout_create_ex.argtypes = [ctypes.POINTER(basp_layout_desc),
+                                          ctypes.POINTER(vp)]
+    lib.basp_layout_create_ex.restype = ctypes.c_int
     lib.basp_layout_query.argtypes = [vp, ctypes.POINTER(basp_info)]
     lib.basp_layout_query.restype = ctypes.c_int
     lib.basp_layout_destroy.argtypes = [vp]
@@ -79,6 +91,10 @@ def load_library():
         fn = getattr(lib, name)
         fn.argtypes = [vp, ctypes.c_int] + [vp] * 6 + [vp, sz, vp, sz, vp]
         fn.restype = ctypes.c_int
+    lib.basp_seq2head_qkv.argtypes = [vp] * 6
+    lib.basp_seq2head_qkv.restype = ctypes.c_int
+    lib.basp_head2seq_qkv.argtypes = [vp] * 6
+    lib.basp_head2seq_qkv.restype = ctypes.c_int
     lib.basp_seq2head_noalloc.argtypes = [vp] + [vp] * 6 + [vp]
     lib.basp_seq2head_noalloc.restype = ctypes.c_int
     lib.basp_status_string.argtypes = [ctypes.c_int]
@@ -121,6 +137,19 @@ def basp_layout_create(B, S, Hq, Hkv, d, N, K, dtype="bf16") -> int:
     _check(load_library().basp_layout_create(B, S, Hq, Hkv, d, N, K, code,
                                              ctypes.byref(h)),
            "basp_layout_create")
+    return h.value
+
+
+def basp_layout_create_ex(B, S, Hq, Hkv, d, N, K, dtype="bf16", order="bshd") -> int:
+    """Create a layout handle with a token order ("bshd" batch-first or
+    "sbhd" sequence-first, or the enum value)."""
+    desc = basp_layout_desc(
+        B, S, Hq, Hkv, d, N, K,
+        DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype),
+        ORDER_CODES[order] if isinstance(order, str) else int(order))
+    h = ctypes.c_void_p()
+    _check(load_library().basp_layout_create_ex(ctypes.byref(desc), ctypes.byref(h)),
+           "basp_layout_create_ex")
     return h.value
 
 
@@ -191,6 +220,20 @@ def basp_head2seq_host(layout, algo, o, k, v, o_out, k_out, v_out, staging,
         _stream(stream)), "basp_head2seq_host")
 
 
+def basp_seq2head_qkv(layout, qkv, q_out, k_out, v_out, stream=None):
+    """Packed seq-sharded QKV -> head-sharded Q, K, V; see ``basp.h``."""
+    _check(load_library().basp_seq2head_qkv(
+        layout, _ptr(qkv), _ptr(q_out), _ptr(k_out), _ptr(v_out),
+        _stream(stream)), "basp_seq2head_qkv")
+
+
+def basp_head2seq_qkv(layout, q, k, v, qkv_out, stream=None):
+    """Head-sharded Q, K, V -> packed seq-sharded QKV; see ``basp.h``."""
+    _check(load_library().basp_head2seq_qkv(
+        layout, _ptr(q), _ptr(k), _ptr(v), _ptr(qkv_out), _stream(stream)),
+        "basp_head2seq_qkv")
+
+
 def basp_seq2head_noalloc(layout, q, k, v, q_out, k_out, v_out, stream=None):
     """seq-sharded -> head-sharded through the three-pass path, using the
     library's built-in scratch instead of a workspace: for callers that cannot
@@ -204,8 +247,8 @@ def basp_seq2head_noalloc(layout, q, k, v, q_out, k_out, v_out, stream=None):
 class Layout:
     """Owns one layout handle; ``info`` holds the derived sizes."""
 
-    def __init__(self, B, S, Hq, Hkv, d, N, K, dtype="bf16"):
-        self.handle = basp_layout_create(B, S, Hq, Hkv, d, N, K, dtype)
+    def __init__(self, B, S, Hq, Hkv, d, N, K, dtype="bf16", order="bshd"):
+        self.handle = basp_layout_create_ex(B, S, Hq, Hkv, d, N, K, dtype, order)
         self.info = basp_layout_query(self.handle)
 
     def close(self):

@@ -24,8 +24,20 @@ extern "C" basp_status basp_layout_create(int64_t B, int64_t S, int64_t Hq,
                                           int64_t Hkv, int64_t d, int64_t N,
                                           int64_t K, basp_dtype dtype,
                                           basp_layout **out) {
+    const basp_layout_desc desc = {B, S, Hq, Hkv, d, N, K, dtype, BASP_ORDER_BSHD};
+    return basp_layout_create_ex(&desc, out);
+}
+
+extern "C" basp_status basp_layout_create_ex(const basp_layout_desc *desc,
+                                             basp_layout **out) {
     if (out == nullptr) return BASP_ERR_INVALID_ARG;
     *out = nullptr;
+    if (desc == nullptr) return BASP_ERR_INVALID_ARG;
+    int64_t B = desc->B, S = desc->S, Hq = desc->Hq, Hkv = desc->Hkv;
+    int64_t d = desc->d, N = desc->N, K = desc->K;
+    const basp_dtype dtype = desc->dtype;
+    if (desc->order != BASP_ORDER_BSHD && desc->order != BASP_ORDER_SBHD)
+        return BASP_ERR_INVALID_ARG;
     int64_t esz;
     switch (dtype) {
         case BASP_DTYPE_BF16: esz = 2; break;
@@ -48,7 +60,7 @@ extern "C" basp_status basp_layout_create(int64_t B, int64_t S, int64_t Hq,
 
     // Every byte offset must fit comfortably in int64 (checked once here so
     // the planners and kernels can multiply freely).
-    const int64_t H = Hq > Hkv ? Hq : Hkv;
+    const int64_t H = Hq + 2 * Hkv;                     // packed QKV row
     int64_t t = 1;
     for (int64_t f : {B, S, H, d, esz, int64_t(4)}) {   // 4: send+recv, in+out
         if (!mul_ok(t, f, &t)) return BASP_ERR_TOO_LARGE;
@@ -63,6 +75,7 @@ extern "C" basp_status basp_layout_create(int64_t B, int64_t S, int64_t Hq,
     L->Sk = S / K;
     L->esz = esz;
     L->dtype = dtype;
+    L->order = desc->order;
     *out = L;
     return BASP_OK;
 }
@@ -86,6 +99,8 @@ extern "C" basp_status basp_layout_query(const basp_layout *L, basp_info *o) {
     o->workspace_bytes = basp::workspace_bytes(*L, H3, 3);
     o->staging_bytes = basp::workspace_bytes(*L, H3, 3);   // inputs + outputs
     o->foil_tokens_per_rank = L->B * L->S / L->K;
+    o->order = L->order;
+    o->bytes_qkv_packed = basp::tensor_bytes(*L, L->Hq + 2 * L->Hkv);
     return BASP_OK;
 }
 

@@ -13,6 +13,7 @@ struct basp_layout {
     int64_t Sk;    // tokens per rank in the seq-sharded layout, S / K
     int64_t esz;   // bytes per element
     basp_dtype dtype;
+    basp_order order;
 };
 
 namespace basp {

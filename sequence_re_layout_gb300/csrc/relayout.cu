@@ -232,34 +232,40 @@ basp_relayout_kernel(const __grid_constant__ Params p) {
 // Host side: stride tables, pass planning, launch.
 // ---------------------------------------------------------------------------
 
-// Strides (in vectors) of the five coordinates for one buffer kind.
-void strides_of(const basp_layout &L, BufKind kind, int64_t vpr, int64_t s[5]) {
+// Strides (in vectors) of the five coordinates for one buffer kind.  `vpr` is
+// the vectors of one row (one rank's head block of one token); `wseq` is the
+// vectors of one whole token row on the seq-sharded side (K * vpr, or the
+// packed QKV row).  Batch-first shards keep a sequence's tokens together;
+// sequence-first shards interleave the group's sequences token by token.
+void strides_of(const basp_layout &L, BufKind kind, int64_t vpr, int64_t wseq,
+                int64_t s[5]) {
     const int64_t K = L.K, Bg = L.Bg, Sk = L.Sk;
+    const bool sf = L.order == BASP_ORDER_SBHD;
     switch (kind) {
-        case SEQ:     // [G][K j][Bg][Sk][K jp][vpr]
+        case SEQ:     // [G][K j][Bg][Sk][row]  or  [G][K j][Sk][Bg][row]
             s[C_JP] = vpr;
-            s[C_SL] = K * vpr;
-            s[C_BL] = Sk * K * vpr;
-            s[C_J] = Bg * Sk * K * vpr;
-            s[C_G] = K * Bg * Sk * K * vpr;
+            s[C_SL] = sf ? Bg * wseq : wseq;
+            s[C_BL] = sf ? wseq : Sk * wseq;
+            s[C_J] = Bg * Sk * wseq;
+            s[C_G] = K * Bg * Sk * wseq;
             break;
-        case HEAD:    // [G][K jp][Bg][K j][Sk][vpr]
-            s[C_SL] = vpr;
-            s[C_J] = Sk * vpr;
-            s[C_BL] = K * Sk * vpr;
+        case HEAD:    // [G][K jp][Bg][K j][Sk][vpr]  or  [G][K jp][K j][Sk][Bg][vpr]
+            s[C_SL] = sf ? Bg * vpr : vpr;
+            s[C_J] = sf ? Sk * Bg * vpr : Sk * vpr;
+            s[C_BL] = sf ? vpr : K * Sk * vpr;
             s[C_JP] = Bg * K * Sk * vpr;
             s[C_G] = K * Bg * K * Sk * vpr;
             break;
-        case BYSRC:   // [G][K j][K jp][Bg][Sk][vpr]
-            s[C_SL] = vpr;
-            s[C_BL] = Sk * vpr;
+        case BYSRC:   // [G][K j][K jp][Bg][Sk][vpr]  or  ...[Sk][Bg][vpr]
+            s[C_SL] = sf ? Bg * vpr : vpr;
+            s[C_BL] = sf ? vpr : Sk * vpr;
             s[C_JP] = Bg * Sk * vpr;
             s[C_J] = K * Bg * Sk * vpr;
             s[C_G] = K * K * Bg * Sk * vpr;
             break;
-        case BYDST:   // [G][K jp][K j][Bg][Sk][vpr]
-            s[C_SL] = vpr;
-            s[C_BL] = Sk * vpr;
+        case BYDST:   // [G][K jp][K j][Bg][Sk][vpr]  or  ...[Sk][Bg][vpr]
+            s[C_SL] = sf ? Bg * vpr : vpr;
+            s[C_BL] = sf ? vpr : Sk * vpr;
             s[C_J] = Bg * Sk * vpr;
             s[C_JP] = K * Bg * Sk * vpr;
             s[C_G] = K * K * Bg * Sk * vpr;
@@ -267,12 +273,15 @@ void strides_of(const basp_layout &L, BufKind kind, int64_t vpr, int64_t s[5]) {
     }
 }
 
+// Extent of a block digit.  In sequence-first order the group's sequences
+// sit next to each other inside every token, so (sl, bl) merge into one row
+// index of S/K * Bg rows whose stride is that of bl, and bl is no digit.
 int64_t extent_of(const basp_layout &L, int c) {
     switch (c) {
         case C_G: return L.G;
         case C_J: return L.K;
         case C_JP: return L.K;
-        case C_BL: return L.Bg;
+        case C_BL: return L.order == BASP_ORDER_SBHD ? 1 : L.Bg;
         default: return L.Sk;
     }
 }
@@ -291,8 +300,14 @@ void udiv_magic(uint32_t D, uint32_t *m, uint32_t *l) {
 struct TensorArg {
     const void *in;
     void *out;
-    int64_t H;
+    int64_t H;       // heads of this tensor
+    int64_t seq_w;   // elements of one token row on the seq-sharded side
+                     // (0: H * d; a packed QKV row is (Hq + 2*Hkv) * d)
 };
+
+int64_t seq_row_elems(const basp_layout &L, const TensorArg &t) {
+    return t.seq_w > 0 ? t.seq_w : t.H * L.d;
+}
 
 struct Pass {
     BufKind from, to;
@@ -326,8 +341,9 @@ int pick_vec(const basp_layout &L, const TensorArg *t, int n,
         bool ok = true;
         for (int i = 0; i < n && ok; ++i) {
             const int64_t row_bytes = (t[i].H / L.K) * L.d * L.esz;
-            ok = fits(uintptr_t(row_bytes)) && fits(uintptr_t(t[i].in)) &&
-                 fits(uintptr_t(t[i].out));
+            const int64_t seq_bytes = seq_row_elems(L, t[i]) * L.esz;
+            ok = fits(uintptr_t(row_bytes)) && fits(uintptr_t(seq_bytes)) &&
+                 fits(uintptr_t(t[i].in)) && fits(uintptr_t(t[i].out));
         }
         for (int i = 0; i < nextra && ok; ++i) ok = fits(uintptr_t(extra[i]));
         if (ok) break;
@@ -344,20 +360,24 @@ basp_status plan(const basp_layout &L, const Pass &pass, const TensorArg *t,
     for (int i = 0; i < n; ++i) {
         const int64_t row_bytes = (t[i].H / L.K) * L.d * L.esz;
         const int64_t vpr = row_bytes / vec;
-        const int64_t vec_per_block = L.Sk * vpr;
+        const int64_t wseq = seq_row_elems(L, t[i]) * L.esz / vec;
+        const bool sf = L.order == BASP_ORDER_SBHD;
+        const int64_t rows = sf ? L.Sk * L.Bg : L.Sk;
+        const int64_t vec_per_block = rows * vpr;
         if (vec_per_block == 0) continue;                    // empty tensor
         if (vec_per_block >= (int64_t(1) << 31)) return BASP_ERR_TOO_LARGE;
         Job &J = p->job[nj++];
         int64_t ss[5], ds[5];
-        strides_of(L, pass.from, vpr, ss);
-        strides_of(L, pass.to, vpr, ds);
+        strides_of(L, pass.from, vpr, wseq, ss);
+        strides_of(L, pass.to, vpr, wseq, ds);
         for (int k = 0; k < 4; ++k) {
             J.src_bs[k] = ss[pass.digit[k]];
             J.dst_bs[k] = ds[pass.digit[k]];
             J.radix[k] = uint32_t(extent_of(L, pass.digit[k]));
         }
-        J.src_rs = ss[C_SL];
-        J.dst_rs = ds[C_SL];
+        // rows: sl (batch-first) or the merged (sl, bl) (sequence-first)
+        J.src_rs = sf ? ss[C_BL] : ss[C_SL];
+        J.dst_rs = sf ? ds[C_BL] : ds[C_SL];
         J.src = static_cast<const unsigned char *>(t[i].in);
         J.dst = static_cast<unsigned char *>(t[i].out);
         J.vpr = uint32_t(vpr);
@@ -366,7 +386,7 @@ basp_status plan(const basp_layout &L, const Pass &pass, const TensorArg *t,
         J.tiles_per_block = uint32_t((vec_per_block + kTileVec - 1) / kTileVec);
         J.tile_begin = uint32_t(tiles);
         J.inner_fast = uint32_t(pass.inner_fast);
-        const uint64_t blocks = uint64_t(L.G) * L.K * L.K * L.Bg;
+        const uint64_t blocks = uint64_t(L.G) * L.K * L.K * uint64_t(extent_of(L, C_BL));
         tiles += blocks * J.tiles_per_block;
         if (tiles >= (uint64_t(1) << 31)) return BASP_ERR_TOO_LARGE;
     }
@@ -551,7 +571,63 @@ basp_status relayout_host(const basp_layout *L, basp_algo algo, bool to_head,
     return BASP_OK;
 }
 
+// Packed QKV: Q, K and V are three jobs of one fused launch whose
+// seq-sharded side is the packed buffer, each starting at its own head offset
+// inside the token row and striding over the whole row.
+basp_status relayout_qkv(const basp_layout *L, bool to_head, const void *packed,
+                         const void *q, const void *k, const void *v,
+                         void *qo, void *ko, void *vo, cudaStream_t stream) {
+    if (L == nullptr || packed == nullptr) return BASP_ERR_INVALID_ARG;
+    const void *ptrs[3] = {to_head ? qo : q, to_head ? ko : k, to_head ? vo : v};
+    for (const void *x : ptrs)
+        if (x == nullptr) return BASP_ERR_INVALID_ARG;
+    for (const void *x : ptrs)
+        if (uintptr_t(x) % uintptr_t(L->esz)) return BASP_ERR_ALIGNMENT;
+    if (uintptr_t(packed) % uintptr_t(L->esz)) return BASP_ERR_ALIGNMENT;
+    const int64_t W = (L->Hq + 2 * L->Hkv) * L->d;
+    const int64_t bytes[3] = {basp::tensor_bytes(*L, L->Hq),
+                              basp::tensor_bytes(*L, L->Hkv),
+                              basp::tensor_bytes(*L, L->Hkv)};
+    const int64_t packed_bytes = basp::tensor_bytes(*L, L->Hq + 2 * L->Hkv);
+    // outputs may overlap neither an input nor each other
+    for (int i = 0; i < 3; ++i) {
+        if (overlaps(ptrs[i], bytes[i], packed, packed_bytes)) return BASP_ERR_ALIASING;
+        if (to_head)
+            for (int j = 0; j < i; ++j)
+                if (overlaps(ptrs[i], bytes[i], ptrs[j], bytes[j])) return BASP_ERR_ALIASING;
+    }
+    const int64_t off[3] = {0, L->Hq * L->d * L->esz, (L->Hq + L->Hkv) * L->d * L->esz};
+    const int64_t H[3] = {L->Hq, L->Hkv, L->Hkv};
+    TensorArg t[3];
+    for (int i = 0; i < 3; ++i) {
+        if (to_head) {
+            t[i] = {static_cast<const unsigned char *>(packed) + off[i],
+                    const_cast<void *>(ptrs[i]), H[i], W};
+        } else {
+            t[i] = {ptrs[i],
+                    static_cast<unsigned char *>(const_cast<void *>(packed)) + off[i],
+                    H[i], W};
+        }
+    }
+    const int vec = pick_vec(*L, t, 3, nullptr, 0);
+    return run_pass(*L, to_head ? kFusedS2H : kFusedH2S, t, 3, vec, stream);
+}
+
 }  // namespace
+
+extern "C" basp_status basp_seq2head_qkv(const basp_layout *L, const void *qkv,
+                                         void *q_out, void *k_out, void *v_out,
+                                         cudaStream_t stream) {
+    return relayout_qkv(L, true, qkv, nullptr, nullptr, nullptr, q_out, k_out,
+                        v_out, stream);
+}
+
+extern "C" basp_status basp_head2seq_qkv(const basp_layout *L, const void *q,
+                                         const void *k, const void *v,
+                                         void *qkv_out, cudaStream_t stream) {
+    return relayout_qkv(L, false, qkv_out, q, k, v, nullptr, nullptr, nullptr,
+                        stream);
+}
 
 extern "C" basp_status basp_seq2head(const basp_layout *L, basp_algo algo,
                                      const void *q, const void *k, const void *v,

@@ -179,3 +179,36 @@ def test_noalloc_size_limit_checked_before_any_cuda_call():
         with pytest.raises(basp.BaspError) as e:
             basp.basp_seq2head_noalloc(L.handle, FAKE, None, None, FAKE + nq, None, None)
         assert e.value.status == basp.BASP_ERR_WORKSPACE
+
+
+def test_create_ex_orders_and_bad_order():
+    h = basp.basp_layout_create_ex(2, 64, 8, 8, 16, 8, 8, "bf16", "sbhd")
+    try:
+        i = basp.basp_layout_query(h)
+        assert i["order"] == basp.BASP_ORDER_SBHD
+        assert i["bytes_qkv_packed"] == 2 * 64 * 24 * 16 * 2
+    finally:
+        basp.basp_layout_destroy(h)
+    with pytest.raises(basp.BaspError) as e:
+        basp.basp_layout_create_ex(2, 64, 8, 8, 16, 8, 8, "bf16", 5)
+    assert e.value.status == basp.BASP_ERR_INVALID_ARG
+
+
+def test_packed_qkv_rejects_before_launch(layout):
+    h = layout.handle
+    nq, nkv = layout.info["bytes_q"], layout.info["bytes_kv"]
+    npk = layout.info["bytes_qkv_packed"]
+    P = FAKE
+    cases = [
+        (lambda: basp.basp_seq2head_qkv(h, P, None, P + npk, P + 2 * npk), basp.BASP_ERR_INVALID_ARG),
+        (lambda: basp.basp_seq2head_qkv(h, P + 1, P + npk, P + 2 * npk, P + 3 * npk), basp.BASP_ERR_ALIGNMENT),
+        (lambda: basp.basp_seq2head_qkv(h, P, P + npk - 2, P + 2 * npk, P + 3 * npk), basp.BASP_ERR_ALIASING),
+        (lambda: basp.basp_seq2head_qkv(h, P, P + npk, P + npk + 16, P + 3 * npk), basp.BASP_ERR_ALIASING),
+        (lambda: basp.basp_head2seq_qkv(h, P, P + nq, P + nq + nkv, P + nq // 2), basp.BASP_ERR_ALIASING),
+        (lambda: basp.basp_head2seq_qkv(h, P, P + nq, P + nq + nkv, None), basp.BASP_ERR_INVALID_ARG),
+        (lambda: basp.basp_head2seq_qkv(0, P, P + nq, P + nq + nkv, P + 4 * npk), basp.BASP_ERR_INVALID_ARG),
+    ]
+    for fn, status in cases:
+        with pytest.raises(basp.BaspError) as e:
+            fn()
+        assert e.value.status == status, e.value
