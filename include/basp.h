@@ -31,6 +31,9 @@
  *     subnormals survive).  bf16 and fp16 are 2-byte words, fp32 4-byte.
  *   - Device pointers must be naturally aligned for the dtype; 16-byte
  *     alignment gives the 16-byte vector path, lesser alignment a narrower one.
+ *   - A "device" buffer may also be page-locked host memory (cudaHostAlloc,
+ *     cudaMallocHost, cudaHostRegister): under unified addressing the kernels
+ *     read and write it in place over the host link, with no staging copy.
  *   - Output ranges may not overlap any input, output or workspace range
  *     (no in-place re-layout): BASP_ERR_ALIASING.
  *   - The caller owns every buffer.  Compute calls allocate nothing, never

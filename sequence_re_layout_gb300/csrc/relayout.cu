@@ -63,6 +63,9 @@ namespace {
 #ifndef BASP_CTAS_PER_SM
 #define BASP_CTAS_PER_SM 0      // 0: as many as fit
 #endif
+#ifndef BASP_PDL
+#define BASP_PDL 0              // 1: programmatic dependent launch
+#endif
 #ifndef BASP_GRID_ALL_TILES
 #define BASP_GRID_ALL_TILES 1   // 0: persistent grid (SMs x resident CTAs)
 #endif
@@ -149,6 +152,13 @@ template <int VEC>
 __global__ void __launch_bounds__(kThreads)
 basp_relayout_kernel(const __grid_constant__ Params p) {
     using W = typename Word<VEC>::T;
+#if BASP_PDL
+    // Launched with programmatic stream serialisation: the previous kernel on
+    // the stream may still be running.  Wait for it (and its memory) before
+    // touching any buffer, then let the next kernel start its own launch.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+#endif
     for (uint32_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
         int jb = 0;
         if (p.njobs > 1 && t >= p.job[1].tile_begin) jb = 1;
@@ -419,7 +429,22 @@ int grid_for(uint32_t tiles) {
 template <int VEC>
 basp_status launch_vec(const Params &p, cudaStream_t stream) {
     const int grid = grid_for<VEC>(p.total_tiles);
+#if BASP_PDL
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, basp_relayout_kernel<VEC>, p) != cudaSuccess)
+        return BASP_ERR_CUDA;
+#else
     basp_relayout_kernel<VEC><<<grid, kThreads, 0, stream>>>(p);
+#endif
     return cudaGetLastError() == cudaSuccess ? BASP_OK : BASP_ERR_CUDA;
 }
 

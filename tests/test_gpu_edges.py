@@ -169,3 +169,23 @@ def test_above_2_to_31_elements_sampled(algo):
         assert torch.equal(z.view(torch.int16), x.view(torch.int16))
     del x, y, z, ws
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_pinned_host_buffers_direct(algo):
+    """basp_seq2head / basp_head2seq on page-locked host buffers: the kernels
+    read and write host memory in place (same pointer on the device under
+    unified addressing)."""
+    B, S, Hq, Hkv, d, N, K = 2, 2048, 32, 8, 64, 8, 4
+    q, k, v, o = make_inputs(B, S, Hq, Hkv, d, "bf16", 37, kind="bits")
+    exp = oracle_outputs(q, k, v, o, B, S, Hq, Hkv, d, N, K)
+    hin = [t.pin_memory() for t in (q, k, v, o)]
+    hout = [torch.empty_like(t).pin_memory() for t in hin]
+    with basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16") as L:
+        ws = torch.empty(L.info["workspace_bytes"], dtype=torch.uint8, device=DEV)
+        basp.basp_seq2head(L.handle, algo, hin[0], hin[1], hin[2],
+                           hout[0], hout[1], hout[2], ws)
+        basp.basp_head2seq(L.handle, algo, hin[3], None, None, hout[3], None, None, ws)
+        torch.cuda.synchronize()
+    for name, g, e in zip("qkvo", hout, exp):
+        np.testing.assert_array_equal(synth_inputs.bits(g), e, err_msg=name)
