@@ -252,22 +252,16 @@ def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
         ws = torch.empty(info["workspace_bytes"], dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(i, ev=None):
+    def step(i):
         ins, outs = sets[i % n_sets]
-        if ev is not None:
-            ev[0].record(stream)
         if packed:
             basp.basp_seq2head_qkv(L.handle, ins[0], outs[0], outs[1], outs[2],
                                    stream=stream)
         else:
             basp.basp_seq2head(L.handle, algo, ins[0], ins[1], ins[2],
                                outs[0], outs[1], outs[2], ws, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
         basp.basp_head2seq(L.handle, algo, ins[3], None, None,
                            outs[3], None, None, ws, stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
 
     for i in range(warmup):
         step(i)
@@ -280,29 +274,51 @@ def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
                 step(i)
                 i += 1
             torch.cuda.synchronize(dev)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
-           for _ in range(steps)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     t0 = time.time()
+    # the timed region: `steps` whole steps back to back, events only around
+    # the loop (events between launches would serialise them)
     start.record(stream)
     for i in range(steps):
-        step(i, evs[i])
+        step(i)
     end.record(stream)
     torch.cuda.synchronize(dev)
     t1 = time.time()
     total_ms = start.elapsed_time(end)
-    s2h = [e[0].elapsed_time(e[1]) for e in evs]
-    h2s = [e[1].elapsed_time(e[2]) for e in evs]
+
+    # roofline: each kernel's average launch duration, `steps` launches of
+    # that kernel alone back to back on the same stream
+    def one_kernel(which):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            ins, outs = sets[i % n_sets]
+            if which == "s2h" and packed:
+                basp.basp_seq2head_qkv(L.handle, ins[0], outs[0], outs[1], outs[2],
+                                       stream=stream)
+            elif which == "s2h":
+                basp.basp_seq2head(L.handle, algo, ins[0], ins[1], ins[2],
+                                   outs[0], outs[1], outs[2], ws, stream=stream)
+            else:
+                basp.basp_head2seq(L.handle, algo, ins[3], None, None,
+                                   outs[3], None, None, ws, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / steps
+
+    s2h_ms = one_kernel("s2h")
+    h2s_ms = one_kernel("h2s")
     launches_per_step = 2 if algo == "fused" else 6
     res = {
         "total_ms": total_ms, "ms_per_step": total_ms / steps,
         "step_bytes": step_bytes, "info": info, "n_sets": n_sets,
-        "l2_bytes": l2, "s2h_ms_mean": statistics.mean(s2h),
-        "h2s_ms_mean": statistics.mean(h2s),
+        "l2_bytes": l2, "s2h_ms_mean": s2h_ms, "h2s_ms_mean": h2s_ms,
         "s2h_bytes": 2 * (info["bytes_q"] + 2 * info["bytes_kv"]),
-        "h2s_bytes": 2 * info["bytes_q"], "launches": launches_per_step * steps,
+        "h2s_bytes": 2 * info["bytes_q"],
+        "launches": 2 * launches_per_step * steps,     # step loop + roofline loops
         "wall": (soak_t0 if soak_s > 0 else t0, t1),
     }
     del sets, ws
@@ -453,6 +469,8 @@ def main_ours(args, dist):
             "frac": round(s2h_gbs / peak, 4), "traffic": traffic,
             "algorithmic_bytes_per_launch": r["s2h_bytes"],
             "launch_ms_mean": round(r["s2h_ms_mean"], 6),
+            "launch_timing": "CUDA events around %d back-to-back launches of "
+                             "this kernel alone on the bench stream" % args.steps,
             "peak_kind": "of %s" % peak_kind,
         },
         "head2seq": {"achieved_gbs": round(gbs(r["h2s_bytes"], r["h2s_ms_mean"]), 2),
@@ -476,6 +494,23 @@ def main_ours(args, dist):
                       "peers_per_rank": ou["peers"],
                       "bytes_per_peer_q": ou["bytes_per_peer_q"],
                       "seq2head_gbs": round(gbs(ru["s2h_bytes"], ru["s2h_ms_mean"]), 2)}
+        if args.layout == "basp" and w.N % w.B == 0:
+            # the review's "trivial alternative" (Strengths, Table I): Ulysses
+            # with SP = N/B, every group of K = N/B ranks holding all B
+            # sequences -- B*B*S/N tokens per rank, B times BASP's bytes
+            from sequence_re_layout_gb300.workloads import Workload
+            wf = Workload(w.name + "_foil", w.B * w.B, w.S, w.Hq, w.Hkv, w.d,
+                          w.N, w.N // w.B, w.dtype)
+            rf = run_device(wf, "basp", args.algo, args.steps, args.warmup, dev,
+                            order=args.order)
+            out["foil_ulysses_sp_n_over_b"] = {
+                "tokens_per_rank": rf["info"]["tokens_per_rank"],
+                "basp_tokens_per_rank": info["tokens_per_rank"],
+                "bytes_per_step": rf["step_bytes"],
+                "ms_per_step": round(rf["ms_per_step"], 6),
+                "value": round(gbs(rf["step_bytes"] * args.steps, rf["total_ms"]), 2),
+                "time_vs_basp": round(rf["ms_per_step"] / (r["total_ms"] / args.steps), 3)}
+            out["gpu_launches"] += rf["launches"]
         alt = "three_pass" if args.algo == "fused" else "fused"
         rt = run_device(w, args.layout, alt, args.steps, args.warmup, dev,
                         order=args.order)

@@ -1,0 +1,80 @@
+"""Host logic of bench.py that needs no GPU: the replica barrier and the
+max/sum reductions over gloo ranks (world size 2), the clock-sample parser,
+the ncu traffic lookup, and the reference arm on a tiny budget."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _dist_worker(rank, world, port, result_dir):
+    os.environ.update({"WORLD_SIZE": str(world), "RANK": str(rank),
+                       "LOCAL_RANK": str(rank), "MASTER_ADDR": "127.0.0.1",
+                       "MASTER_PORT": str(port)})
+    d = bench.Dist()
+    d.barrier()
+    mx = d.max(float(rank + 1) * 10.0)
+    sm = d.sum(float(rank + 1))
+    d.close()
+    with open(os.path.join(result_dir, "r%d" % rank), "w") as f:
+        json.dump({"max": mx, "sum": sm}, f)
+
+
+def test_replica_reductions_over_gloo(tmp_path):
+    mp.spawn(_dist_worker, args=(2, _free_port(), str(tmp_path)), nprocs=2, join=True)
+    for r in range(2):
+        got = json.load(open(tmp_path / ("r%d" % r)))
+        assert got == {"max": 20.0, "sum": 3.0}
+
+
+def test_clock_summary_parses_nvidia_smi_lines():
+    cs = bench.ClockSampler.__new__(bench.ClockSampler)
+    cs.proc = object()
+    cs.lines = [
+        "2026/12/02 10:00:00.100, 2070, 2070, 500.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:00:00.300, 1980, 2070, 800.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 10:00:05.000, 300, 2070, 90.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    import datetime as dt
+    t0 = dt.datetime(2026, 12, 2, 10, 0, 0).timestamp()
+    s = cs.summary(t0, t0 + 1.0)
+    assert s["samples"] == 2 and s["sm_mhz"] == 2025.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_traffic_lookup_tracks_the_kernel_source(tmp_path, monkeypatch):
+    f = tmp_path / "t.txt"
+    f.write_text("traffic wl basp seq2head_qkv_fused bytes=123 source=%s\n"
+                 "traffic wl basp head2seq_o_fused bytes=7 source=0000\n"
+                 % bench.source_digest())
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.ncu_traffic("wl", "basp", "seq2head_qkv_fused") == 123.0
+    assert bench.ncu_traffic("wl", "basp", "head2seq_o_fused") is None   # stale
+    assert bench.ncu_traffic("other", "basp", "seq2head_qkv_fused") is None
+
+
+def test_reference_arm_prints_one_line():
+    """--impl reference: the oracle on the host cores, one JSON line."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl",
+                        "reference", "--steps", "2", "--warmup", "1",
+                        "--config", "llama3.2-3b_B2_S1024"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s"
+    assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0

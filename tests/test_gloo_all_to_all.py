@@ -85,3 +85,45 @@ def test_gloo_all_to_all_matches_oracle(shape, tmp_path):
             ok_y, ok_z = f.read().split()
         assert ok_y == "1", "rank %d: all-to-all result differs from oracle" % r
         assert ok_z == "1", "rank %d: inverse all-to-all did not restore input" % r
+
+
+def _dropout_worker(rank, world, port, result_dir):
+    """Rank 1 leaves before the exchange; rank 0 must see an error from its
+    all-to-all within the process group's timeout instead of hanging."""
+    import datetime
+    import time
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=5))
+    if rank == 1:
+        os._exit(0)                      # dies between steps, nothing in flight
+    t0 = time.time()
+    outcome = "completed"
+    try:
+        x = torch.zeros(8)
+        y = torch.empty_like(x)
+        dist.all_to_all_single(y, x)
+    except Exception as e:               # gloo reports the lost peer
+        outcome = "error:" + type(e).__name__
+    with open(os.path.join(result_dir, "r0"), "w") as f:
+        f.write("%s %.1f" % (outcome, time.time() - t0))
+    os._exit(0)
+
+
+def test_lost_rank_is_reported_not_hung(tmp_path):
+    ctx = mp.get_context("spawn")
+    port = _free_port()
+    procs = [ctx.Process(target=_dropout_worker, args=(r, 2, port, str(tmp_path)))
+             for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    for p in procs:
+        if p.is_alive():
+            p.kill()
+            pytest.fail("a rank hung after its peer left")
+    outcome, secs = open(tmp_path / "r0").read().split()
+    assert outcome.startswith("error:"), outcome
+    assert float(secs) < 60
