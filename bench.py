@@ -36,7 +36,7 @@ METRIC = ("seq↔head re-layout GB/s (read+write) and % of GB300 HBM peak, "
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
-KERNEL_SOURCE = os.path.join(ROOT, "sequence_re_layout_gb300", "csrc", "relayout.cu")
+KERNEL_SOURCE = os.path.join(ROOT, "sequence_re_layout_gb300", "csrc", "relayout_kernel.cuh")
 
 
 def parse_args():
@@ -46,7 +46,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--config", default=None)
     p.add_argument("--layout", default="basp", choices=["basp", "ulysses"])
-    p.add_argument("--algo", default="fused", choices=["fused", "three_pass"])
+    p.add_argument("--algo", default="fused",
+                   choices=["fused", "three_pass", "three_pass_elide"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--order", default="bshd", choices=["bshd", "sbhd"],
                    help="token order inside the shards (batch- or sequence-first)")
@@ -248,7 +249,7 @@ def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
     n_sets = min(4096, max(2, -(-4 * l2 // step_bytes) + 1))   # >= 4x L2 per rotation
     sets = _alloc_sets(w, K, w.dtype, n_sets, dev, 1234, packed)
     ws = None
-    if algo == "three_pass":
+    if algo != "fused":
         ws = torch.empty(info["workspace_bytes"], dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -311,7 +312,10 @@ def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
 
     s2h_ms = one_kernel("s2h")
     h2s_ms = one_kernel("h2s")
-    launches_per_step = 2 if algo == "fused" else 6
+    passes = {"fused": 1, "three_pass": 3}.get(algo)
+    if passes is None:                 # three_pass_elide
+        passes = 2 if (info["seqs_per_group"] == 1 or order == "sbhd") else 3
+    launches_per_step = 2 * passes
     res = {
         "total_ms": total_ms, "ms_per_step": total_ms / steps,
         "step_bytes": step_bytes, "info": info, "n_sets": n_sets,
@@ -346,7 +350,7 @@ def run_e2e(w, layout, algo, steps, warmup, dev, mode="staged"):
     hout = [torch.empty_like(t).pin_memory() for t in hin]
     staging = torch.empty(info["staging_bytes"], dtype=torch.uint8, device=dev)
     ws = None
-    if algo == "three_pass":
+    if algo != "fused":
         ws = torch.empty(info["workspace_bytes"], dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -511,14 +515,21 @@ def main_ours(args, dist):
                 "value": round(gbs(rf["step_bytes"] * args.steps, rf["total_ms"]), 2),
                 "time_vs_basp": round(rf["ms_per_step"] / (r["total_ms"] / args.steps), 3)}
             out["gpu_launches"] += rf["launches"]
-        alt = "three_pass" if args.algo == "fused" else "fused"
-        rt = run_device(w, args.layout, alt, args.steps, args.warmup, dev,
-                        order=args.order)
-        vt = gbs(rt["step_bytes"] * args.steps, rt["total_ms"])
-        out[alt] = {"value": round(vt, 2), "ms_per_step": round(rt["ms_per_step"], 6),
-                    "pct_hbm_peak": round(100 * vt / peak, 2),
-                    "note": "same algorithmic bytes; the three passes move them 3x"}
-        out["gpu_launches"] += ru["launches"] + rt["launches"]
+        out["gpu_launches"] += ru["launches"]
+        alts = [a for a in ("fused", "three_pass", "three_pass_elide") if a != args.algo]
+        notes = {"three_pass": "same algorithmic bytes; the three passes move them 3x",
+                 "three_pass_elide": "identity pass skipped when the receive chunks "
+                                     "are already head-sharded (2 passes here: %s)"
+                                     % ("yes" if info["seqs_per_group"] == 1 or
+                                        args.order == "sbhd" else "no"),
+                 "fused": "one pass"}
+        for alt in alts:
+            rt = run_device(w, args.layout, alt, args.steps, args.warmup, dev,
+                            order=args.order)
+            vt = gbs(rt["step_bytes"] * args.steps, rt["total_ms"])
+            out[alt] = {"value": round(vt, 2), "ms_per_step": round(rt["ms_per_step"], 6),
+                        "pct_hbm_peak": round(100 * vt / peak, 2), "note": notes[alt]}
+            out["gpu_launches"] += rt["launches"]
         ne = max(3, min(args.steps, 50))
         e = run_e2e(w, args.layout, args.algo, ne, 3, dev, mode="direct")
         es = run_e2e(w, args.layout, args.algo, ne, 3, dev, mode="staged")
@@ -532,7 +543,7 @@ def main_ours(args, dist):
                                  "ms_per_step": round(es["ms_per_step"], 4),
                                  "api": "basp_seq2head_host + basp_head2seq_host "
                                         "(H2D copy, re-layout, D2H copy)"}}
-        out["gpu_launches"] += 2 * 2 * ne * (1 if args.algo == "fused" else 3)
+        out["gpu_launches"] += 2 * ne * r["launches"] // (2 * args.steps)
         if dist.world == 1:
             out["cpu_baseline"] = cpu_baseline(w, args.layout, args.cpu_baseline_s)
     if dist.rank == 0:

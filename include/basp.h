@@ -79,7 +79,15 @@ typedef enum basp_algo {
      * contiguous send chunks, exchange the chunks between the members of each
      * group (recv chunk j of member j' = send chunk j' of member j, the
      * equal-split all-to-all convention), unpack.  Needs a workspace. */
-    BASP_ALGO_THREE_PASS = 1
+    BASP_ALGO_THREE_PASS = 1,
+    /* The three-pass path with the pass skipped that is the identity: when
+     * each group holds one sequence (every BASP layout) or the order is
+     * sequence-first, the receive chunks already sit in head-sharded order,
+     * so seq2head exchanges straight into its output and head2seq exchanges
+     * straight from its input (two passes, workspace of one region per
+     * tensor).  Otherwise it runs all three passes like
+     * BASP_ALGO_THREE_PASS. */
+    BASP_ALGO_THREE_PASS_ELIDE = 2
 } basp_algo;
 
 typedef enum basp_status {

@@ -10,7 +10,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libbasp.so")
 SOURCES = ["layout.cpp", "relayout.cu"]
-HEADERS = [os.path.join(INCLUDE, "basp.h"), os.path.join(CSRC, "layout_internal.h")]
+HEADERS = [os.path.join(INCLUDE, "basp.h"), os.path.join(CSRC, "layout_internal.h"),
+           os.path.join(CSRC, "relayout_kernel.cuh")]
 
 NVCC_FLAGS = [
     "-O3", "-std=c++17",

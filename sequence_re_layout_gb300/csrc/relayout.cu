@@ -49,198 +49,9 @@
 #include <mutex>
 
 #include "layout_internal.h"
+#include "relayout_kernel.cuh"
 
 namespace {
-
-#ifndef BASP_THREADS
-#define BASP_THREADS 256
-#endif
-#ifndef BASP_UNROLL
-#define BASP_UNROLL 4
-#endif
-#ifndef BASP_STORE_CS
-#define BASP_STORE_CS 1
-#endif
-#ifndef BASP_RECOMPUTE_DST
-#define BASP_RECOMPUTE_DST 0
-#endif
-#ifndef BASP_CTAS_PER_SM
-#define BASP_CTAS_PER_SM 0      // 0: as many as fit
-#endif
-#ifndef BASP_PDL
-#define BASP_PDL 1              // programmatic dependent launch (0: plain launch)
-#endif
-#ifndef BASP_GRID_ALL_TILES
-#define BASP_GRID_ALL_TILES 1   // 0: persistent grid (SMs x resident CTAs)
-#endif
-constexpr int kThreads = BASP_THREADS;   // threads per CTA
-constexpr int kUnroll = BASP_UNROLL;     // vectors in flight per thread
-constexpr int kTileVec = kThreads * kUnroll;
-constexpr int kMaxJobs = 3;
-
-enum Coord { C_G = 0, C_J = 1, C_JP = 2, C_BL = 3, C_SL = 4 };
-enum BufKind { SEQ, HEAD, BYSRC, BYDST };
-
-// One tensor's share of one launch.
-struct Job {
-    const unsigned char *src;
-    unsigned char *dst;
-    int64_t src_bs[4], dst_bs[4];   // block-digit strides, in vectors
-    int64_t src_rs, dst_rs;         // row strides, in vectors
-    uint32_t radix[4];              // block-digit radices; digit 3 fastest
-    uint32_t vpr;                   // vectors per row
-    uint32_t vpr_magic, vpr_shift;  // i / vpr == (umulhi(i, magic) + i) >> shift
-    uint32_t vec_per_block;         // rows * vpr  (< 2^31)
-    uint32_t tiles_per_block;
-    uint32_t tile_begin;            // first tile of this job within the launch
-    uint32_t inner_fast;            // 1: digit 3 varies fastest across tiles
-};
-
-struct Params {
-    Job job[kMaxJobs];
-    int njobs;
-    uint32_t total_tiles;
-};
-
-template <int VEC> struct Word;
-template <> struct Word<16> { using T = uint4; };
-template <> struct Word<8> { using T = uint2; };
-template <> struct Word<4> { using T = uint32_t; };
-template <> struct Word<2> { using T = unsigned short; };
-
-__device__ __forceinline__ uint4 load_stream(const uint4 *p) {
-    uint4 v;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint2 load_stream(const uint2 *p) {
-    uint2 v;
-    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
-        : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint32_t load_stream(const uint32_t *p) {
-    uint32_t v;
-    asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ unsigned short load_stream(const unsigned short *p) {
-    unsigned short v;
-    asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
-    return v;
-}
-
-#if BASP_STORE_CS
-#define BASP_ST "st.global.cs"
-#else
-#define BASP_ST "st.global"
-#endif
-
-__device__ __forceinline__ void store(uint4 *p, uint4 v) {
-    asm volatile(BASP_ST ".v4.u32 [%0], {%1, %2, %3, %4};"
-                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
-}
-__device__ __forceinline__ void store(uint2 *p, uint2 v) {
-    asm volatile(BASP_ST ".v2.u32 [%0], {%1, %2};"
-                 :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
-}
-__device__ __forceinline__ void store(uint32_t *p, uint32_t v) {
-    asm volatile(BASP_ST ".u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void store(unsigned short *p, unsigned short v) {
-    asm volatile(BASP_ST ".u16 [%0], %1;" :: "l"(p), "h"(v) : "memory");
-}
-
-template <int VEC>
-__global__ void __launch_bounds__(kThreads)
-basp_relayout_kernel(const __grid_constant__ Params p) {
-    using W = typename Word<VEC>::T;
-#if BASP_PDL
-    // Launched with programmatic stream serialisation: the previous kernel on
-    // the stream may still be running.  Wait for it (and its memory) before
-    // touching any buffer, then let the next kernel start its own launch.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" :::);
-#endif
-    for (uint32_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-        int jb = 0;
-        if (p.njobs > 1 && t >= p.job[1].tile_begin) jb = 1;
-        if (p.njobs > 2 && t >= p.job[2].tile_begin) jb = 2;
-        const Job &J = p.job[jb];
-
-        // tile -> (block digits, tile within block).  Tiles run either block
-        // by block (inner_fast = 0) or with the innermost block digit varying
-        // fastest, so that consecutive tiles fill neighbouring row segments.
-        uint32_t lt = t - J.tile_begin;
-        uint32_t tb, q;
-        int64_t sb = 0, db = 0;
-        if (J.inner_fast) {
-            q = lt / J.radix[3];
-            const uint32_t d3 = lt - q * J.radix[3];
-            sb += int64_t(d3) * J.src_bs[3];
-            db += int64_t(d3) * J.dst_bs[3];
-            lt = q;
-            q = lt / J.tiles_per_block;
-            tb = lt - q * J.tiles_per_block;
-            lt = q;
-        } else {
-            q = lt / J.tiles_per_block;
-            tb = lt - q * J.tiles_per_block;
-            lt = q;
-            q = lt / J.radix[3];
-            const uint32_t d3 = lt - q * J.radix[3];
-            sb += int64_t(d3) * J.src_bs[3];
-            db += int64_t(d3) * J.dst_bs[3];
-            lt = q;
-        }
-#pragma unroll
-        for (int k = 2; k >= 1; --k) {
-            q = lt / J.radix[k];
-            const uint32_t dgt = lt - q * J.radix[k];
-            sb += int64_t(dgt) * J.src_bs[k];
-            db += int64_t(dgt) * J.dst_bs[k];
-            lt = q;
-        }
-        sb += int64_t(lt) * J.src_bs[0];
-        db += int64_t(lt) * J.dst_bs[0];
-
-        const uint32_t i0 = tb * uint32_t(kTileVec);
-        const uint32_t i1 = min(i0 + uint32_t(kTileVec), J.vec_per_block);
-        const W *src = reinterpret_cast<const W *>(J.src) + sb;
-        W *dst = reinterpret_cast<W *>(J.dst) + db;
-
-        W v[kUnroll];
-#if !BASP_RECOMPUTE_DST
-        int64_t doff[kUnroll];
-#endif
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const uint32_t i = i0 + threadIdx.x + uint32_t(u * kThreads);
-            if (i < i1) {
-                const uint32_t row = (__umulhi(i, J.vpr_magic) + i) >> J.vpr_shift;
-                const uint32_t col = i - row * J.vpr;
-                v[u] = load_stream(src + (int64_t(row) * J.src_rs + col));
-#if !BASP_RECOMPUTE_DST
-                doff[u] = int64_t(row) * J.dst_rs + col;
-#endif
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const uint32_t i = i0 + threadIdx.x + uint32_t(u * kThreads);
-            if (i < i1) {
-#if BASP_RECOMPUTE_DST
-                const uint32_t row = (__umulhi(i, J.vpr_magic) + i) >> J.vpr_shift;
-                const uint32_t col = i - row * J.vpr;
-                store(dst + (int64_t(row) * J.dst_rs + col), v[u]);
-#else
-                store(dst + doff[u], v[u]);
-#endif
-            }
-        }
-    }
-}
 
 // ---------------------------------------------------------------------------
 // Host side: stride tables, pass planning, launch.
@@ -507,6 +318,52 @@ int64_t region_bytes(const basp_layout &L, const TensorArg *t, int n) {
     return basp::workspace_bytes(L, H, n);
 }
 
+// True when the receive-chunk layout of the three-pass path addresses every
+// row exactly as the head-sharded layout does (one sequence per group, or
+// sequence-first order): the unpack of seq2head and the pack of head2seq are
+// then the identity and can be skipped.
+bool recv_chunks_are_head_sharded(const basp_layout &L) {
+    int64_t a[5], b[5];
+    strides_of(L, BYDST, 1, L.K, a);
+    strides_of(L, HEAD, 1, L.K, b);
+    const bool sf = L.order == BASP_ORDER_SBHD;
+    const int64_t ext[5] = {L.G, L.K, L.K, sf ? L.Sk * L.Bg : L.Bg, sf ? 1 : L.Sk};
+    for (int c = 0; c < 5; ++c)
+        if (ext[c] > 1 && a[c] != b[c]) return false;
+    return true;
+}
+
+// The three-pass path with its identity pass skipped: seq2head packs into the
+// workspace and exchanges straight into the head-sharded output; head2seq
+// exchanges the head-sharded input into the workspace and unpacks from there.
+// Needs one workspace region per tensor.
+basp_status relayout_two_pass(const basp_layout &L, bool to_head,
+                              const TensorArg *t, int n, void *ws,
+                              size_t ws_bytes, cudaStream_t stream) {
+    int64_t need = 0;
+    for (int i = 0; i < n; ++i) need += basp::align256(basp::tensor_bytes(L, t[i].H));
+    if (need > 0 && (ws == nullptr || int64_t(ws_bytes) < need))
+        return BASP_ERR_WORKSPACE;
+    for (int i = 0; i < n; ++i) {
+        const int64_t b = basp::tensor_bytes(L, t[i].H);
+        if (overlaps(ws, need, t[i].in, b) || overlaps(ws, need, t[i].out, b))
+            return BASP_ERR_ALIASING;
+    }
+    if (uintptr_t(ws) % uintptr_t(L.esz)) return BASP_ERR_ALIGNMENT;
+    TensorArg first[3], second[3];
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    for (int i = 0; i < n; ++i) {
+        first[i] = {t[i].in, w, t[i].H};
+        second[i] = {w, t[i].out, t[i].H};
+        w += basp::align256(basp::tensor_bytes(L, t[i].H));
+    }
+    const void *extra[1] = {ws};
+    const int vec = pick_vec(L, t, n, extra, 1);
+    basp_status st = run_pass(L, to_head ? kPackS2H : kExchH2S, first, n, vec, stream);
+    if (st != BASP_OK) return st;
+    return run_pass(L, to_head ? kExchS2H : kUnpackH2S, second, n, vec, stream);
+}
+
 basp_status relayout(const basp_layout *L, basp_algo algo, bool to_head,
                      const void *a, const void *k, const void *v, void *ao,
                      void *ko, void *vo, void *ws, size_t ws_bytes,
@@ -519,7 +376,10 @@ basp_status relayout(const basp_layout *L, basp_algo algo, bool to_head,
         const int vec = pick_vec(*L, t, n, nullptr, 0);
         return run_pass(*L, to_head ? kFusedS2H : kFusedH2S, t, n, vec, stream);
     }
-    if (algo != BASP_ALGO_THREE_PASS) return BASP_ERR_INVALID_ARG;
+    if (algo != BASP_ALGO_THREE_PASS && algo != BASP_ALGO_THREE_PASS_ELIDE)
+        return BASP_ERR_INVALID_ARG;
+    if (algo == BASP_ALGO_THREE_PASS_ELIDE && recv_chunks_are_head_sharded(*L))
+        return relayout_two_pass(*L, to_head, t, n, ws, ws_bytes, stream);
 
     const int64_t need = region_bytes(*L, t, n);
     if (need > 0 && (ws == nullptr || int64_t(ws_bytes) < need))

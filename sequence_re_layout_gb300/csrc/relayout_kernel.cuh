@@ -1,0 +1,209 @@
+// relayout_kernel.cuh -- device side of the re-layout: the one copy kernel
+// every pass launches, its job table and its load/store helpers.  Included
+// once, by relayout.cu.
+//
+// Each CTA copies one tile of kThreads * kUnroll vectors (16 KiB at 16-byte
+// vectors).  A tile lies inside one block of rows (fixed g, j, jp, bl); the
+// block's source and destination bases come from its four digits times the
+// job's stride tables, and vector i of the block sits in row i / vpr,
+// column i % vpr.  Loads are non-coherent and skip L1; stores are
+// evict-first.  Every thread issues its kUnroll loads before its stores.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace {
+
+#ifndef BASP_THREADS
+#define BASP_THREADS 256
+#endif
+#ifndef BASP_UNROLL
+#define BASP_UNROLL 4
+#endif
+#ifndef BASP_STORE_CS
+#define BASP_STORE_CS 1
+#endif
+#ifndef BASP_RECOMPUTE_DST
+#define BASP_RECOMPUTE_DST 0
+#endif
+#ifndef BASP_CTAS_PER_SM
+#define BASP_CTAS_PER_SM 0      // 0: as many as fit
+#endif
+#ifndef BASP_PDL
+#define BASP_PDL 1              // programmatic dependent launch (0: plain launch)
+#endif
+#ifndef BASP_GRID_ALL_TILES
+#define BASP_GRID_ALL_TILES 1   // 0: persistent grid (SMs x resident CTAs)
+#endif
+constexpr int kThreads = BASP_THREADS;   // threads per CTA
+constexpr int kUnroll = BASP_UNROLL;     // vectors in flight per thread
+constexpr int kTileVec = kThreads * kUnroll;
+constexpr int kMaxJobs = 3;
+
+enum Coord { C_G = 0, C_J = 1, C_JP = 2, C_BL = 3, C_SL = 4 };
+enum BufKind { SEQ, HEAD, BYSRC, BYDST };
+
+// One tensor's share of one launch.
+struct Job {
+    const unsigned char *src;
+    unsigned char *dst;
+    int64_t src_bs[4], dst_bs[4];   // block-digit strides, in vectors
+    int64_t src_rs, dst_rs;         // row strides, in vectors
+    uint32_t radix[4];              // block-digit radices; digit 3 fastest
+    uint32_t vpr;                   // vectors per row
+    uint32_t vpr_magic, vpr_shift;  // i / vpr == (umulhi(i, magic) + i) >> shift
+    uint32_t vec_per_block;         // rows * vpr  (< 2^31)
+    uint32_t tiles_per_block;
+    uint32_t tile_begin;            // first tile of this job within the launch
+    uint32_t inner_fast;            // 1: digit 3 varies fastest across tiles
+};
+
+struct Params {
+    Job job[kMaxJobs];
+    int njobs;
+    uint32_t total_tiles;
+};
+
+template <int VEC> struct Word;
+template <> struct Word<16> { using T = uint4; };
+template <> struct Word<8> { using T = uint2; };
+template <> struct Word<4> { using T = uint32_t; };
+template <> struct Word<2> { using T = unsigned short; };
+
+__device__ __forceinline__ uint4 load_stream(const uint4 *p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 load_stream(const uint2 *p) {
+    uint2 v;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+        : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t load_stream(const uint32_t *p) {
+    uint32_t v;
+    asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ unsigned short load_stream(const unsigned short *p) {
+    unsigned short v;
+    asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+#if BASP_STORE_CS
+#define BASP_ST "st.global.cs"
+#else
+#define BASP_ST "st.global"
+#endif
+
+__device__ __forceinline__ void store(uint4 *p, uint4 v) {
+    asm volatile(BASP_ST ".v4.u32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ void store(uint2 *p, uint2 v) {
+    asm volatile(BASP_ST ".v2.u32 [%0], {%1, %2};"
+                 :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+__device__ __forceinline__ void store(uint32_t *p, uint32_t v) {
+    asm volatile(BASP_ST ".u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void store(unsigned short *p, unsigned short v) {
+    asm volatile(BASP_ST ".u16 [%0], %1;" :: "l"(p), "h"(v) : "memory");
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kThreads)
+basp_relayout_kernel(const __grid_constant__ Params p) {
+    using W = typename Word<VEC>::T;
+#if BASP_PDL
+    // Launched with programmatic stream serialisation: the previous kernel on
+    // the stream may still be running.  Wait for it (and its memory) before
+    // touching any buffer, then let the next kernel start its own launch.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+#endif
+    for (uint32_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        int jb = 0;
+        if (p.njobs > 1 && t >= p.job[1].tile_begin) jb = 1;
+        if (p.njobs > 2 && t >= p.job[2].tile_begin) jb = 2;
+        const Job &J = p.job[jb];
+
+        // tile -> (block digits, tile within block).  Tiles run either block
+        // by block (inner_fast = 0) or with the innermost block digit varying
+        // fastest, so that consecutive tiles fill neighbouring row segments.
+        uint32_t lt = t - J.tile_begin;
+        uint32_t tb, q;
+        int64_t sb = 0, db = 0;
+        if (J.inner_fast) {
+            q = lt / J.radix[3];
+            const uint32_t d3 = lt - q * J.radix[3];
+            sb += int64_t(d3) * J.src_bs[3];
+            db += int64_t(d3) * J.dst_bs[3];
+            lt = q;
+            q = lt / J.tiles_per_block;
+            tb = lt - q * J.tiles_per_block;
+            lt = q;
+        } else {
+            q = lt / J.tiles_per_block;
+            tb = lt - q * J.tiles_per_block;
+            lt = q;
+            q = lt / J.radix[3];
+            const uint32_t d3 = lt - q * J.radix[3];
+            sb += int64_t(d3) * J.src_bs[3];
+            db += int64_t(d3) * J.dst_bs[3];
+            lt = q;
+        }
+#pragma unroll
+        for (int k = 2; k >= 1; --k) {
+            q = lt / J.radix[k];
+            const uint32_t dgt = lt - q * J.radix[k];
+            sb += int64_t(dgt) * J.src_bs[k];
+            db += int64_t(dgt) * J.dst_bs[k];
+            lt = q;
+        }
+        sb += int64_t(lt) * J.src_bs[0];
+        db += int64_t(lt) * J.dst_bs[0];
+
+        const uint32_t i0 = tb * uint32_t(kTileVec);
+        const uint32_t i1 = min(i0 + uint32_t(kTileVec), J.vec_per_block);
+        const W *src = reinterpret_cast<const W *>(J.src) + sb;
+        W *dst = reinterpret_cast<W *>(J.dst) + db;
+
+        W v[kUnroll];
+#if !BASP_RECOMPUTE_DST
+        int64_t doff[kUnroll];
+#endif
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint32_t i = i0 + threadIdx.x + uint32_t(u * kThreads);
+            if (i < i1) {
+                const uint32_t row = (__umulhi(i, J.vpr_magic) + i) >> J.vpr_shift;
+                const uint32_t col = i - row * J.vpr;
+                v[u] = load_stream(src + (int64_t(row) * J.src_rs + col));
+#if !BASP_RECOMPUTE_DST
+                doff[u] = int64_t(row) * J.dst_rs + col;
+#endif
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint32_t i = i0 + threadIdx.x + uint32_t(u * kThreads);
+            if (i < i1) {
+#if BASP_RECOMPUTE_DST
+                const uint32_t row = (__umulhi(i, J.vpr_magic) + i) >> J.vpr_shift;
+                const uint32_t col = i - row * J.vpr;
+                store(dst + (int64_t(row) * J.dst_rs + col), v[u]);
+#else
+                store(dst + doff[u], v[u]);
+#endif
+            }
+        }
+    }
+}
+
+}  // namespace

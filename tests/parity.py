@@ -44,7 +44,7 @@ def device_outputs(q, k, v, o, B, S, Hq, Hkv, d, N, K, dtype, algo,
     outs = [torch.empty_like(t) for t in (qd, kd, vd, od)]
     with basp.Layout(B, S, Hq, Hkv, d, N, K, dtype) as L:
         ws = None
-        if algo == "three_pass":
+        if algo != "fused":
             ws = torch.empty(max(L.info["workspace_bytes"], 1), dtype=torch.uint8,
                              device=dev)
         s = stream or torch.cuda.current_stream()

@@ -212,3 +212,19 @@ def test_packed_qkv_rejects_before_launch(layout):
         with pytest.raises(basp.BaspError) as e:
             fn()
         assert e.value.status == status, e.value
+
+
+def test_three_pass_elide_workspace_rule():
+    """With one sequence per group the elided path needs one workspace region
+    per tensor (not two) and refuses less."""
+    with basp.Layout(2, 64, 8, 4, 16, 4, 2, "bf16") as L:      # BASP: Bg = 1
+        nq = L.info["bytes_q"]
+        h = L.handle
+        with pytest.raises(basp.BaspError) as e:
+            basp.basp_seq2head(h, "three_pass_elide", FAKE, None, None, FAKE + nq,
+                               None, None, FAKE + 4 * nq, nq - 1)
+        assert e.value.status == basp.BASP_ERR_WORKSPACE
+        with pytest.raises(basp.BaspError) as e:
+            basp.basp_seq2head(h, "three_pass_elide", FAKE, None, None, FAKE + nq,
+                               None, None, FAKE + nq // 2, nq)
+        assert e.value.status == basp.BASP_ERR_ALIASING

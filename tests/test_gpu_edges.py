@@ -13,7 +13,7 @@ from parity import (assert_bits_equal, device_outputs, make_inputs,
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
-ALGOS = ("fused", "three_pass")
+ALGOS = ("fused", "three_pass", "three_pass_elide")
 
 
 @pytest.mark.parametrize("shape", [
@@ -65,7 +65,7 @@ def test_alignment_fallbacks_and_guard_bands(offset, algo):
         raws.append((raw, a, b))
     with basp.Layout(B, S, Hq, Hkv, d, N, K, dtype) as L:
         ws = wraw = None
-        if algo == "three_pass":
+        if algo != "fused":
             ws, wraw, wa, wb = _padded(L.info["workspace_bytes"], torch.uint8,
                                        offset, 0x3C)
         basp.basp_seq2head(L.handle, algo, ins[0], ins[1], ins[2],
@@ -152,7 +152,7 @@ def test_above_2_to_31_elements_sampled(algo):
     y = torch.empty_like(x)
     with basp.Layout(B, S, H, 8, d, N, K, "bf16") as L:
         ws = None
-        if algo == "three_pass":
+        if algo != "fused":
             ws = torch.empty(2 * L.info["bytes_q"] + 512, dtype=torch.uint8, device=DEV)
         basp.basp_seq2head(L.handle, algo, x, None, None, y, None, None, ws)
         torch.cuda.synchronize()
@@ -189,3 +189,41 @@ def test_pinned_host_buffers_direct(algo):
         torch.cuda.synchronize()
     for name, g, e in zip("qkvo", hout, exp):
         np.testing.assert_array_equal(synth_inputs.bits(g), e, err_msg=name)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_cuda_graph_capture_and_replay(algo):
+    """The entry points allocate nothing and never synchronise, so a step
+    (seq2head Q,K,V + head2seq O) can be captured into a CUDA graph and
+    replayed; the programmatic launches become graph edges.  Replays on new
+    input contents give the oracle's bits."""
+    B, S, Hq, Hkv, d, N, K = 2, 1024, 32, 8, 64, 8, 4
+    shapes = (B * S * Hq * d, B * S * Hkv * d, B * S * Hkv * d, B * S * Hq * d)
+    ins = [torch.empty(n, dtype=torch.bfloat16, device=DEV) for n in shapes]
+    outs = [torch.empty_like(t) for t in ins]
+    with basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16") as L:
+        ws = torch.empty(L.info["workspace_bytes"], dtype=torch.uint8, device=DEV)
+        s = torch.cuda.Stream()
+
+        def step():
+            basp.basp_seq2head(L.handle, algo, ins[0], ins[1], ins[2],
+                               outs[0], outs[1], outs[2], ws, stream=s)
+            basp.basp_head2seq(L.handle, algo, ins[3], None, None, outs[3],
+                               None, None, ws, stream=s)
+
+        with torch.cuda.stream(s):
+            step()                                  # first call outside capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step()
+        for seed in (3, 4):
+            q, k, v, o = make_inputs(B, S, Hq, Hkv, d, "bf16", seed, kind="bits")
+            for dst, src in zip(ins, (q, k, v, o)):
+                dst.copy_(src.to(DEV))
+            torch.cuda.synchronize()
+            g.replay()
+            torch.cuda.synchronize()
+            exp = oracle_outputs(q, k, v, o, B, S, Hq, Hkv, d, N, K)
+            for name, got, e in zip("qkvo", outs, exp):
+                assert_bits_equal(got, e, "graph %s seed %d %s" % (algo, seed, name))

@@ -14,7 +14,7 @@ from sequence_re_layout_gb300.workloads import WORKLOADS
 
 pytestmark = pytest.mark.gpu
 
-ALGOS = ("fused", "three_pass")
+ALGOS = ("fused", "three_pass", "three_pass_elide")
 
 
 def _shapes():

@@ -12,7 +12,7 @@ from sequence_re_layout_gb300.workloads import WORKLOADS
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
-ALGOS = ("fused", "three_pass")
+ALGOS = ("fused", "three_pass", "three_pass_elide")
 
 
 def _run_sf(shape, dtype, seed=41, kind="bits"):
