@@ -335,8 +335,8 @@ def run_e2e(w, layout, algo, steps, warmup, dev, mode="staged"):
     """Same step with the tensors in pinned host memory, inside the timed
     region every step.  mode "staged": basp_seq2head_host / basp_head2seq_host
     copy the inputs to device staging, re-lay out, copy the results back.
-    mode "direct": basp_seq2head / basp_head2seq get the pinned host buffers
-    themselves; the kernels read and write host memory over the host link."""
+    mode "direct": the same calls without staging; the kernels read and write
+    the pinned host buffers in place over the host link."""
     import torch
     import synth_inputs
     import sequence_re_layout_gb300 as basp
@@ -356,10 +356,11 @@ def run_e2e(w, layout, algo, steps, warmup, dev, mode="staged"):
 
     def step():
         if mode == "direct":
-            basp.basp_seq2head(L.handle, algo, hin[0], hin[1], hin[2],
-                               hout[0], hout[1], hout[2], ws, stream=stream)
-            basp.basp_head2seq(L.handle, algo, hin[3], None, None, hout[3],
-                               None, None, ws, stream=stream)
+            basp.basp_seq2head_host(L.handle, algo, hin[0], hin[1], hin[2],
+                                    hout[0], hout[1], hout[2], None, 0,
+                                    workspace=ws, stream=stream)
+            basp.basp_head2seq_host(L.handle, algo, hin[3], None, None, hout[3],
+                                    None, None, None, 0, workspace=ws, stream=stream)
             return
         basp.basp_seq2head_host(L.handle, algo, hin[0], hin[1], hin[2],
                                 hout[0], hout[1], hout[2], staging,
@@ -537,12 +538,13 @@ def main_ours(args, dist):
                       "unit": "GB/s", "h2d_bytes_per_step": e["bytes_in"],
                       "d2h_bytes_per_step": e["bytes_out"],
                       "ms_per_step": round(e["ms_per_step"], 4),
-                      "api": "basp_seq2head + basp_head2seq on pinned host buffers "
-                             "(kernels read and write host memory directly)",
+                      "api": "basp_seq2head_host + basp_head2seq_host, direct mode "
+                             "(no staging: kernels read and write the pinned host "
+                             "buffers in place)",
                       "staged": {"value": round(gbs(es["step_bytes"], es["ms_per_step"]), 2),
                                  "ms_per_step": round(es["ms_per_step"], 4),
-                                 "api": "basp_seq2head_host + basp_head2seq_host "
-                                        "(H2D copy, re-layout, D2H copy)"}}
+                                 "api": "basp_seq2head_host + basp_head2seq_host, "
+                                        "staged mode (H2D copy, re-layout, D2H copy)"}}
         out["gpu_launches"] += 2 * ne * r["launches"] // (2 * args.steps)
         if dist.world == 1:
             out["cpu_baseline"] = cpu_baseline(w, args.layout, args.cpu_baseline_s)

@@ -43,6 +43,13 @@
  *     a failed launch or copy on `stream`.
  *   - A layout handle is immutable after creation; calls that share one
  *     handle may run concurrently from several host threads.
+ *   - Kernels are launched with programmatic dependent launch: they may be
+ *     scheduled while the previous kernel on `stream` drains, but wait for it
+ *     (and its memory) before touching any buffer, so ordering on `stream` is
+ *     as usual.  They also release the next kernel early; a kernel the caller
+ *     launches after them with the programmatic-serialisation attribute must
+ *     wait (cudaGridDependencySynchronize) before reading their outputs, as
+ *     CUDA requires of every such kernel.
  */
 #ifndef BASP_H
 #define BASP_H
@@ -221,12 +228,18 @@ basp_status basp_head2seq_qkv(const basp_layout *layout, const void *q,
                               cudaStream_t stream);
 
 /*
- * End-to-end forms for callers whose tensors live in host memory: enqueue on
- * `stream` the host->device copies of the given inputs into `staging`, the
- * re-layout, and the device->host copies of the results into the host output
- * pointers.  `staging` is caller-owned device memory of at least
- * info.staging_bytes.  Host pointers should be page-locked for the copies to
- * overlap; the host outputs are valid once `stream` has been synchronised.
+ * End-to-end forms for callers whose tensors live in host memory; the host
+ * outputs are valid once `stream` has been synchronised.  Two modes:
+ *   staged  (`staging` given): enqueue on `stream` the host->device copies of
+ *           the inputs into `staging`, the re-layout, and the device->host
+ *           copies of the results.  `staging` is caller-owned device memory
+ *           of at least info.staging_bytes; host pointers should be
+ *           page-locked for the copies to run asynchronously.
+ *   direct  (`staging` NULL): every host buffer must be page-locked
+ *           (cudaHostAlloc, cudaMallocHost, cudaHostRegister), else
+ *           BASP_ERR_WORKSPACE; the kernels read the inputs and write the
+ *           outputs in place over the host link, with no copies.  On GB300
+ *           (NVLink-C2C) this is the faster mode.
  * Arguments otherwise as for basp_seq2head / basp_head2seq.
  */
 basp_status basp_seq2head_host(const basp_layout *layout, basp_algo algo,

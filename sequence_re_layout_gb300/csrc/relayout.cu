@@ -221,7 +221,7 @@ basp_status plan(const basp_layout &L, const Pass &pass, const TensorArg *t,
 }
 
 template <int VEC>
-int grid_for(uint32_t tiles) {
+int grid_for(uint32_t tiles, bool persistent) {
     // Persistent grid: every SM filled to its resident-CTA limit, cached per
     // device (a benign race: every thread computes the same numbers).
     static std::atomic<int> cache[64];
@@ -237,13 +237,13 @@ int grid_for(uint32_t tiles) {
         slots = (sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
         cache[dev].store(slots, std::memory_order_relaxed);
     }
-    if (BASP_GRID_ALL_TILES) return int(tiles);
+    if (BASP_GRID_ALL_TILES && !persistent) return int(tiles);
     return int(tiles < uint32_t(slots) ? tiles : uint32_t(slots));
 }
 
 template <int VEC>
-basp_status launch_vec(const Params &p, cudaStream_t stream) {
-    const int grid = grid_for<VEC>(p.total_tiles);
+basp_status launch_vec(const Params &p, cudaStream_t stream, bool persistent) {
+    const int grid = grid_for<VEC>(p.total_tiles, persistent);
 #if BASP_PDL
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid));
@@ -264,15 +264,16 @@ basp_status launch_vec(const Params &p, cudaStream_t stream) {
 }
 
 basp_status run_pass(const basp_layout &L, const Pass &pass,
-                     const TensorArg *t, int n, int vec, cudaStream_t stream) {
+                     const TensorArg *t, int n, int vec, cudaStream_t stream,
+                     bool persistent = false) {
     Params p;
     basp_status st = plan(L, pass, t, n, vec, &p);
     if (st != BASP_OK || p.total_tiles == 0) return st;
     switch (vec) {
-        case 16: return launch_vec<16>(p, stream);
-        case 8: return launch_vec<8>(p, stream);
-        case 4: return launch_vec<4>(p, stream);
-        default: return launch_vec<2>(p, stream);
+        case 16: return launch_vec<16>(p, stream, persistent);
+        case 8: return launch_vec<8>(p, stream, persistent);
+        case 4: return launch_vec<4>(p, stream, persistent);
+        default: return launch_vec<2>(p, stream, persistent);
     }
 }
 
@@ -339,7 +340,8 @@ bool recv_chunks_are_head_sharded(const basp_layout &L) {
 // Needs one workspace region per tensor.
 basp_status relayout_two_pass(const basp_layout &L, bool to_head,
                               const TensorArg *t, int n, void *ws,
-                              size_t ws_bytes, cudaStream_t stream) {
+                              size_t ws_bytes, cudaStream_t stream,
+                              bool persistent) {
     int64_t need = 0;
     for (int i = 0; i < n; ++i) need += basp::align256(basp::tensor_bytes(L, t[i].H));
     if (need > 0 && (ws == nullptr || int64_t(ws_bytes) < need))
@@ -359,27 +361,30 @@ basp_status relayout_two_pass(const basp_layout &L, bool to_head,
     }
     const void *extra[1] = {ws};
     const int vec = pick_vec(L, t, n, extra, 1);
-    basp_status st = run_pass(L, to_head ? kPackS2H : kExchH2S, first, n, vec, stream);
+    basp_status st = run_pass(L, to_head ? kPackS2H : kExchH2S, first, n, vec, stream,
+                              persistent);
     if (st != BASP_OK) return st;
-    return run_pass(L, to_head ? kExchS2H : kUnpackH2S, second, n, vec, stream);
+    return run_pass(L, to_head ? kExchS2H : kUnpackH2S, second, n, vec, stream,
+                    persistent);
 }
 
 basp_status relayout(const basp_layout *L, basp_algo algo, bool to_head,
                      const void *a, const void *k, const void *v, void *ao,
                      void *ko, void *vo, void *ws, size_t ws_bytes,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, bool persistent = false) {
     TensorArg t[3];
     int n = 0;
     basp_status st = collect(L, a, k, v, ao, ko, vo, t, &n);
     if (st != BASP_OK) return st;
     if (algo == BASP_ALGO_FUSED) {
         const int vec = pick_vec(*L, t, n, nullptr, 0);
-        return run_pass(*L, to_head ? kFusedS2H : kFusedH2S, t, n, vec, stream);
+        return run_pass(*L, to_head ? kFusedS2H : kFusedH2S, t, n, vec, stream,
+                        persistent);
     }
     if (algo != BASP_ALGO_THREE_PASS && algo != BASP_ALGO_THREE_PASS_ELIDE)
         return BASP_ERR_INVALID_ARG;
     if (algo == BASP_ALGO_THREE_PASS_ELIDE && recv_chunks_are_head_sharded(*L))
-        return relayout_two_pass(*L, to_head, t, n, ws, ws_bytes, stream);
+        return relayout_two_pass(*L, to_head, t, n, ws, ws_bytes, stream, persistent);
 
     const int64_t need = region_bytes(*L, t, n);
     if (need > 0 && (ws == nullptr || int64_t(ws_bytes) < need))
@@ -408,7 +413,7 @@ basp_status relayout(const basp_layout *L, basp_algo algo, bool to_head,
                              to_head ? &kUnpackS2H : &kUnpackH2S};
     const TensorArg *args[3] = {pack, exch, unpack};
     for (int s = 0; s < 3; ++s) {
-        st = run_pass(*L, *passes[s], args[s], n, vec, stream);
+        st = run_pass(*L, *passes[s], args[s], n, vec, stream, persistent);
         if (st != BASP_OK) return st;
     }
     return BASP_OK;
@@ -424,7 +429,29 @@ basp_status relayout_host(const basp_layout *L, basp_algo algo, bool to_head,
     basp_status st = collect(L, a, k, v, ao, ko, vo, t, &n);
     if (st != BASP_OK) return st;
     const int64_t need = region_bytes(*L, t, n);
-    if (need > 0 && (staging == nullptr || int64_t(staging_bytes) < need))
+    if (staging == nullptr && need > 0) {
+        // Direct: every host buffer must be page-locked; the kernels reach it
+        // through its device address (the same address under unified
+        // addressing).  A persistent grid keeps more bytes in flight over the
+        // host link than one tile per CTA.
+        const void *hp[6] = {a, k, v, ao, ko, vo};
+        const void *dp[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+        for (int x = 0; x < 6; ++x) {
+            if (hp[x] == nullptr) continue;
+            cudaPointerAttributes attr;
+            if (cudaPointerGetAttributes(&attr, hp[x]) != cudaSuccess) {
+                cudaGetLastError();
+                return BASP_ERR_WORKSPACE;
+            }
+            if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr)
+                return BASP_ERR_WORKSPACE;
+            dp[x] = attr.devicePointer;
+        }
+        return relayout(L, algo, to_head, dp[0], dp[1], dp[2],
+                        const_cast<void *>(dp[3]), const_cast<void *>(dp[4]),
+                        const_cast<void *>(dp[5]), ws, ws_bytes, stream, true);
+    }
+    if (need > 0 && int64_t(staging_bytes) < need)
         return BASP_ERR_WORKSPACE;
     if (overlaps(staging, need, ws, int64_t(ws_bytes))) return BASP_ERR_ALIASING;
     // staging regions: [in 0][out 0][in 1][out 1]...

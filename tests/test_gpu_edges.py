@@ -227,3 +227,30 @@ def test_cuda_graph_capture_and_replay(algo):
             exp = oracle_outputs(q, k, v, o, B, S, Hq, Hkv, d, N, K)
             for name, got, e in zip("qkvo", outs, exp):
                 assert_bits_equal(got, e, "graph %s seed %d %s" % (algo, seed, name))
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_host_entry_points_direct_mode(algo):
+    """basp_*_host without staging: page-locked host buffers are re-laid out in
+    place by the kernels; a pageable buffer is refused before any launch."""
+    B, S, Hq, Hkv, d, N, K = 2, 2048, 32, 8, 64, 8, 4
+    q, k, v, o = make_inputs(B, S, Hq, Hkv, d, "bf16", 43, kind="bits")
+    exp = oracle_outputs(q, k, v, o, B, S, Hq, Hkv, d, N, K)
+    hin = [t.pin_memory() for t in (q, k, v, o)]
+    hout = [torch.empty_like(t).pin_memory() for t in hin]
+    with basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16") as L:
+        ws = torch.empty(L.info["workspace_bytes"], dtype=torch.uint8, device=DEV)
+        st = torch.cuda.current_stream()
+        basp.basp_seq2head_host(L.handle, algo, hin[0], hin[1], hin[2],
+                                hout[0], hout[1], hout[2], None, 0,
+                                workspace=ws, stream=st)
+        basp.basp_head2seq_host(L.handle, algo, hin[3], None, None, hout[3],
+                                None, None, None, 0, workspace=ws, stream=st)
+        st.synchronize()
+        pageable = torch.empty_like(q)
+        with pytest.raises(basp.BaspError) as e:
+            basp.basp_seq2head_host(L.handle, algo, hin[0], None, None, pageable,
+                                    None, None, None, 0, workspace=ws, stream=st)
+        assert e.value.status == basp.BASP_ERR_WORKSPACE
+    for name, g, e in zip("qkvo", hout, exp):
+        np.testing.assert_array_equal(synth_inputs.bits(g), e, err_msg=name)
