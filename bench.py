@@ -53,6 +53,8 @@ def parse_args():
                    help="token order inside the shards (batch- or sequence-first)")
     p.add_argument("--qkv-packed", action="store_true",
                    help="seq2head reads one packed QKV projection output")
+    p.add_argument("--graph", action="store_true",
+                   help="capture each step into a CUDA graph and replay it")
     p.add_argument("--soak-s", type=float, default=1.0,
                    help="untimed seconds at full load before the timed region "
                         "(so the clock samples see the loaded GPU)")
@@ -235,7 +237,7 @@ def _alloc_sets(w, K, dtype, n_sets, dev, seed, packed=False):
 
 
 def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
-               packed=False):
+               packed=False, graph=False):
     """Time `steps` steps of the hot path; returns a dict of timings."""
     import torch
     import sequence_re_layout_gb300 as basp
@@ -263,6 +265,26 @@ def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
                                outs[0], outs[1], outs[2], ws, stream=stream)
         basp.basp_head2seq(L.handle, algo, ins[3], None, None,
                            outs[3], None, None, ws, stream=stream)
+
+    if graph:
+        # one step per buffer set captured into a CUDA graph (on a side
+        # stream, as capture requires); the graphs replay on the bench stream
+        eager = step
+        for i in range(n_sets):
+            eager(i)                                   # first calls eagerly
+        torch.cuda.synchronize(dev)
+        gs = []
+        cap = torch.cuda.Stream(dev)
+        for i in range(n_sets):
+            g = torch.cuda.CUDAGraph()
+            stream = cap
+            with torch.cuda.graph(g, stream=cap):
+                eager(i)
+            gs.append(g)
+        stream = torch.cuda.current_stream(dev)
+
+        def step(i):
+            gs[i % n_sets].replay()
 
     for i in range(warmup):
         step(i)
@@ -436,7 +458,8 @@ def main_ours(args, dist):
     if args.qkv_packed and args.algo != "fused":
         raise SystemExit("--qkv-packed runs the fused path only")
     r = run_device(w, args.layout, args.algo, args.steps, args.warmup, dev,
-                   soak_s=args.soak_s, order=args.order, packed=args.qkv_packed)
+                   soak_s=args.soak_s, order=args.order, packed=args.qkv_packed,
+                   graph=args.graph)
     sampler.stop()
     dist.barrier()
     t_max = dist.max(r["total_ms"])
@@ -458,6 +481,7 @@ def main_ours(args, dist):
         "config": {
             "workload": w.name, "layout": args.layout, "algo": args.algo,
             "order": args.order, "qkv_packed": bool(args.qkv_packed),
+            "cuda_graph": bool(args.graph),
             "B": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "N": w.N,
             "K": info["K"], "groups": info["groups"],
             "bytes_per_step": r["step_bytes"],
