@@ -1,5 +1,6 @@
-// relayout.cu -- the seq-sharded <-> head-sharded re-layout kernels for
-// sm_103a and the C-ABI entry points that plan and launch them.
+// relayout.cu -- host side of the seq-sharded <-> head-sharded re-layout:
+// stride tables, pass planning, launch, and the C-ABI entry points.  The one
+// device kernel every pass launches is in relayout_kernel.cuh.
 //
 // The operation is the all-to-all of Ulysses / BASP attention (review "BASP:
 // Communication-Efficient Batch-Aware Sequence Parallelism for LLM Training",
@@ -15,32 +16,26 @@
 //     jp member holding the heads   (K)   -- head-sharded owner
 //     bl sequence within the group  (Bg = B/G)
 //     sl token within the block     (S/K)
-// and each buffer kind is a stride table over them:
+// and each buffer kind is a stride table over them (batch-first order shown;
+// sequence-first order swaps [Bg] and [S/K] inside every table):
 //     SEQ   seq-sharded  [G][K j][Bg][S/K sl][K jp][L]
 //     HEAD  head-sharded [G][K jp][Bg][K j][S/K sl][L]
 //     BYSRC send chunks  [G][K j][K jp][Bg][S/K][L]   (chunk jp of rank g*K+j)
 //     BYDST recv chunks  [G][K jp][K j][Bg][S/K][L]   (slot j of rank g*K+jp)
 // A pass copies every row from one kind to another.  The fused path is one
 // pass SEQ -> HEAD (or back); the three-pass path is pack (SEQ -> BYSRC),
-// exchange (BYSRC -> BYDST, whole chunks), unpack (BYDST -> HEAD).
+// exchange (BYSRC -> BYDST, whole chunks), unpack (BYDST -> HEAD), with the
+// identity pass skipped on request when BYDST and HEAD address rows alike.
+// Packed QKV input is three jobs whose SEQ rows stride over the packed row.
 //
-// One kernel serves every pass.  Each CTA copies one "tile" of
-// kThreads * kUnroll 16-byte vectors (16 KiB); a tile belongs to one "block"
-// (fixed g, j, jp, bl: S/K rows), whose source and destination base offsets
-// come from the two stride tables; inside the block, vector i sits in row
-// i / vpr, column i % vpr (vpr = vectors per row; the division uses the
-// Granlund-Montgomery multiply-high method for invariant divisors, "Division by
-// Invariant Integers using Multiplication", PLDI 1994).  Loads are
-// non-coherent streaming loads that skip L1, stores are evict-first; each
-// thread keeps kUnroll independent 16-byte loads in flight before it stores.
-// One tile per CTA (rather than a persistent grid striding over tiles) measured
-// 5-12% faster on GB300: retiring CTAs let new ones start their loads while
-// others drain their stores.  Launches use programmatic dependent launch: a
-// kernel's CTAs may be scheduled while the previous kernel on the stream
-// drains, and wait (griddepcontrol.wait) for it to finish before touching
-// memory, which hides the launch gap between back-to-back re-layouts
-// (3-10% per step on GB300).  No shared memory, no tensor cores: the work is
-// pure data movement, bounded by HBM bandwidth.
+// Launch policy (all measured on GB300): one 16 KiB tile per CTA rather than
+// a persistent grid (5-12% faster on HBM: retiring CTAs let new ones start
+// their loads while others drain their stores), except for page-locked host
+// buffers, where a persistent grid keeps more bytes in flight over the host
+// link; programmatic dependent launch, so a kernel's CTAs may be scheduled
+// while the previous kernel on the stream drains (each waits with
+// griddepcontrol.wait before touching memory), hiding the launch gap between
+// back-to-back re-layouts (3-10% per step).
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -222,8 +217,9 @@ basp_status plan(const basp_layout &L, const Pass &pass, const TensorArg *t,
 
 template <int VEC>
 int grid_for(uint32_t tiles, bool persistent) {
-    // Persistent grid: every SM filled to its resident-CTA limit, cached per
-    // device (a benign race: every thread computes the same numbers).
+    // One CTA per tile, or (persistent) every SM filled to its resident-CTA
+    // limit with the CTAs striding over the tiles.  The slot count is cached
+    // per device (a benign race: every thread computes the same numbers).
     static std::atomic<int> cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
@@ -284,7 +280,8 @@ bool overlaps(const void *a, int64_t na, const void *b, int64_t nb) {
 }
 
 // Gather the (input, output, heads) triples of one call and check pairing,
-// alignment and aliasing.  `first_H` is Hq (Q or O); the other two are Hkv.
+// alignment and aliasing.  The first pair has Hq heads (Q or O), the other
+// two Hkv (K, V).
 basp_status collect(const basp_layout *L, const void *a, const void *k,
                     const void *v, void *ao, void *ko, void *vo,
                     TensorArg *t, int *n) {

@@ -16,6 +16,14 @@
 
 namespace {
 
+// Build-time tuning switches (-DBASP_...=); the defaults are the settings
+// that measured best on GB300.  None of them changes what is copied where.
+//   BASP_THREADS, BASP_UNROLL  tile shape: threads per CTA, vectors per thread
+//   BASP_STORE_CS              evict-first stores (1) or plain stores (0)
+//   BASP_RECOMPUTE_DST         recompute store offsets instead of keeping them
+//   BASP_CTAS_PER_SM           cap on resident CTAs for persistent grids
+//   BASP_PDL                   programmatic dependent launch
+//   BASP_GRID_ALL_TILES        one CTA per tile (1) or a persistent grid (0)
 #ifndef BASP_THREADS
 #define BASP_THREADS 256
 #endif
