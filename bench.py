@@ -190,8 +190,18 @@ class ClockSampler:
 
 
 def source_digest():
-    with open(KERNEL_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Digest of the kernel source's code: comments and blank space removed,
+    so a comment edit does not orphan a traffic record."""
+    import re
+    with open(KERNEL_SOURCE) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    code = []
+    for line in text.splitlines():
+        line = line.split("//", 1)[0].strip()
+        if line:
+            code.append(" ".join(line.split()))
+    return hashlib.sha256("\n".join(code).encode()).hexdigest()[:16]
 
 
 def ncu_traffic(workload: str, layout: str, kernel_role: str):
