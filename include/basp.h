@@ -28,7 +28,8 @@
  *
  * Conventions for every call below.
  *   - Elements are copied bit for bit (no rounding; NaN payloads, -0 and
- *     subnormals survive).  bf16 and fp16 are 2-byte words, fp32 4-byte.
+ *     subnormals survive).  fp8 is a 1-byte word, bf16 and fp16 2-byte,
+ *     fp32 4-byte.
  *   - Device pointers must be naturally aligned for the dtype; 16-byte
  *     alignment gives the 16-byte vector path, lesser alignment a narrower one.
  *   - A "device" buffer may also be page-locked host memory (cudaHostAlloc,
@@ -65,7 +66,8 @@ extern "C" {
 typedef enum basp_dtype {
     BASP_DTYPE_BF16 = 0,
     BASP_DTYPE_FP32 = 1,
-    BASP_DTYPE_FP16 = 2
+    BASP_DTYPE_FP16 = 2,
+    BASP_DTYPE_FP8 = 3      /* any 1-byte format (e4m3, e5m2, int8), copied as bytes */
 } basp_dtype;
 
 /* Token order inside every rank shard.  The pages fix none; batch-first is the

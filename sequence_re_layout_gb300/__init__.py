@@ -3,7 +3,7 @@ attention activations as hand-written CUDA for sm_103a behind a C ABI
 (``include/basp.h``), with a thin ctypes binding of the same names."""
 from .binding import (  # noqa: F401
     ALGO_CODES, BASP_ALGO_FUSED, BASP_ALGO_THREE_PASS, BASP_ALGO_THREE_PASS_ELIDE, BASP_DTYPE_BF16,
-    BASP_DTYPE_FP16, BASP_DTYPE_FP32, BASP_ERR_ALIASING, BASP_ERR_ALIGNMENT,
+    BASP_DTYPE_FP16, BASP_DTYPE_FP32, BASP_DTYPE_FP8, BASP_ERR_ALIASING, BASP_ERR_ALIGNMENT,
     BASP_ERR_BATCH_GT_RANKS, BASP_ERR_CUDA, BASP_ERR_DIVISIBILITY,
     BASP_ERR_INVALID_ARG, BASP_ERR_TOO_LARGE, BASP_ERR_WORKSPACE, BASP_OK,
     DTYPE_CODES, EXPORTS, ORDER_CODES, BASP_ORDER_BSHD, BASP_ORDER_SBHD,

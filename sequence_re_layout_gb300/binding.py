@@ -14,7 +14,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libbasp.so")
 
 # enums of basp.h
-BASP_DTYPE_BF16, BASP_DTYPE_FP32, BASP_DTYPE_FP16 = 0, 1, 2
+BASP_DTYPE_BF16, BASP_DTYPE_FP32, BASP_DTYPE_FP16, BASP_DTYPE_FP8 = 0, 1, 2, 3
 BASP_ALGO_FUSED, BASP_ALGO_THREE_PASS, BASP_ALGO_THREE_PASS_ELIDE = 0, 1, 2
 BASP_ORDER_BSHD, BASP_ORDER_SBHD = 0, 1
 (BASP_OK, BASP_ERR_INVALID_ARG, BASP_ERR_DIVISIBILITY, BASP_ERR_BATCH_GT_RANKS,
@@ -22,7 +22,7 @@ BASP_ORDER_BSHD, BASP_ORDER_SBHD = 0, 1
  BASP_ERR_TOO_LARGE) = range(9)
 
 DTYPE_CODES = {"bf16": BASP_DTYPE_BF16, "fp32": BASP_DTYPE_FP32,
-               "fp16": BASP_DTYPE_FP16}
+               "fp16": BASP_DTYPE_FP16, "fp8": BASP_DTYPE_FP8}
 ALGO_CODES = {"fused": BASP_ALGO_FUSED, "three_pass": BASP_ALGO_THREE_PASS,
               "three_pass_elide": BASP_ALGO_THREE_PASS_ELIDE}
 ORDER_CODES = {"bshd": BASP_ORDER_BSHD, "sbhd": BASP_ORDER_SBHD}

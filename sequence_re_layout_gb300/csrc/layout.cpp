@@ -42,6 +42,7 @@ extern "C" basp_status basp_layout_create_ex(const basp_layout_desc *desc,
     switch (dtype) {
         case BASP_DTYPE_BF16: esz = 2; break;
         case BASP_DTYPE_FP16: esz = 2; break;
+        case BASP_DTYPE_FP8: esz = 1; break;
         case BASP_DTYPE_FP32: esz = 4; break;
         default: return BASP_ERR_INVALID_ARG;
     }

@@ -269,7 +269,8 @@ basp_status run_pass(const basp_layout &L, const Pass &pass,
         case 16: return launch_vec<16>(p, stream, persistent);
         case 8: return launch_vec<8>(p, stream, persistent);
         case 4: return launch_vec<4>(p, stream, persistent);
-        default: return launch_vec<2>(p, stream, persistent);
+        case 2: return launch_vec<2>(p, stream, persistent);
+        default: return launch_vec<1>(p, stream, persistent);
     }
 }
 

@@ -79,6 +79,7 @@ template <> struct Word<16> { using T = uint4; };
 template <> struct Word<8> { using T = uint2; };
 template <> struct Word<4> { using T = uint32_t; };
 template <> struct Word<2> { using T = unsigned short; };
+template <> struct Word<1> { using T = unsigned char; };
 
 __device__ __forceinline__ uint4 load_stream(const uint4 *p) {
     uint4 v;
@@ -96,6 +97,11 @@ __device__ __forceinline__ uint32_t load_stream(const uint32_t *p) {
     uint32_t v;
     asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
+}
+__device__ __forceinline__ unsigned char load_stream(const unsigned char *p) {
+    unsigned short v;
+    asm("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(v) : "l"(p));
+    return static_cast<unsigned char>(v);
 }
 __device__ __forceinline__ unsigned short load_stream(const unsigned short *p) {
     unsigned short v;
@@ -119,6 +125,10 @@ __device__ __forceinline__ void store(uint2 *p, uint2 v) {
 }
 __device__ __forceinline__ void store(uint32_t *p, uint32_t v) {
     asm volatile(BASP_ST ".u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void store(unsigned char *p, unsigned char v) {
+    const unsigned short w = v;
+    asm volatile(BASP_ST ".u8 [%0], %1;" :: "l"(p), "h"(w) : "memory");
 }
 __device__ __forceinline__ void store(unsigned short *p, unsigned short v) {
     asm volatile(BASP_ST ".u16 [%0], %1;" :: "l"(p), "h"(v) : "memory");

@@ -21,6 +21,7 @@ DTYPES = {
     "bf16": torch.bfloat16,
     "fp16": torch.float16,
     "fp32": torch.float32,
+    "fp8": torch.float8_e4m3fn,
 }
 
 # numpy view types for comparing raw bits
@@ -28,6 +29,7 @@ BITS = {
     torch.bfloat16: torch.int16,
     torch.float16: torch.int16,
     torch.float32: torch.int32,
+    torch.float8_e4m3fn: torch.int8,
 }
 
 

@@ -25,10 +25,10 @@ def _random_case(rng):
     Hkv = K * rng.randint(1, 3)
     Hq = Hkv * rng.choice([1, 2, 3, 4])
     d = rng.choice([1, 2, 3, 8, 16, 24, 64, 80, 128])
-    dtype = rng.choice(["bf16", "fp16", "fp32"])
+    dtype = rng.choice(["bf16", "fp16", "fp32", "fp8"])
     order = rng.choice(["bshd", "sbhd"])
     algo = rng.choice(["fused", "three_pass", "three_pass_elide"])
-    esz = 4 if dtype == "fp32" else 2
+    esz = {"fp32": 4, "fp8": 1}.get(dtype, 2)
     offset = rng.choice([0, 0, esz, 2 * esz, 8]) // esz * esz
     return (B, S, Hq, Hkv, d, N, K), dtype, order, algo, offset
 

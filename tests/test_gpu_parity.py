@@ -74,7 +74,7 @@ SMALL = [
 
 
 @pytest.mark.parametrize("shape", SMALL)
-@pytest.mark.parametrize("dtype", ["bf16", "fp32", "fp16"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32", "fp16", "fp8"])
 def test_small_shapes(shape, dtype):
     B, S, Hq, Hkv, d, N, K = shape
     q, k, v, o = make_inputs(B, S, Hq, Hkv, d, dtype, 99, kind="bits")
@@ -83,3 +83,10 @@ def test_small_shapes(shape, dtype):
         got = device_outputs(q, k, v, o, *shape, dtype, algo)
         for name, g, e in zip("qkvo", got, exp):
             assert_bits_equal(g, e, "%s %s %s %s" % (shape, dtype, algo, name))
+
+
+@pytest.mark.parametrize("name", ["llama3.2-1b_B2_S8192", "llama3.2-3b_B2_S32768"])
+@pytest.mark.parametrize("layout", ["basp", "ulysses"])
+def test_full_size_fp8(name, layout):
+    """1-byte elements (fp8 activations): the 1-byte word is never split."""
+    _check(WORKLOADS[name], "fp8", layout)
