@@ -9,5 +9,5 @@ from .binding import (  # noqa: F401
     DTYPE_CODES, EXPORTS, ORDER_CODES, BASP_ORDER_BSHD, BASP_ORDER_SBHD,
     basp_layout_create_ex, basp_seq2head_qkv, basp_head2seq_qkv, BaspError, Layout, basp_head2seq, basp_head2seq_host,
     basp_layout_create, basp_layout_destroy, basp_layout_query, basp_seq2head,
-    basp_seq2head_host, basp_seq2head_noalloc, basp_status_string,
+    basp_seq2head_host, basp_seq2head_noalloc, basp_debug_bounds_violations, basp_status_string,
     BASP_NOALLOC_SCRATCH_BYTES, load_library)

@@ -11,7 +11,9 @@ import ctypes
 import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libbasp.so")
+# BASP_LIBRARY=debug selects the bounds-checking build (libbasp_debug.so)
+LIB_PATH = os.path.join(PKG, "libbasp_debug.so" if os.environ.get("BASP_LIBRARY") == "debug"
+                        else "libbasp.so")
 
 # enums of basp.h
 BASP_DTYPE_BF16, BASP_DTYPE_FP32, BASP_DTYPE_FP16, BASP_DTYPE_FP8 = 0, 1, 2, 3
@@ -98,6 +100,9 @@ def load_library():
     lib.basp_head2seq_qkv.restype = ctypes.c_int
     lib.basp_seq2head_noalloc.argtypes = [vp] + [vp] * 6 + [vp]
     lib.basp_seq2head_noalloc.restype = ctypes.c_int
+    if hasattr(lib, "basp_debug_bounds_violations"):
+        lib.basp_debug_bounds_violations.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
+        lib.basp_debug_bounds_violations.restype = ctypes.c_int
     lib.basp_status_string.argtypes = [ctypes.c_int]
     lib.basp_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -219,6 +224,18 @@ def basp_head2seq_host(layout, algo, o, k, v, o_out, k_out, v_out, staging,
         layout, _algo(algo), _ptr(o), _ptr(k), _ptr(v), _ptr(o_out),
         _ptr(k_out), _ptr(v_out), _ptr(staging), sb, _ptr(workspace), wb,
         _stream(stream)), "basp_head2seq_host")
+
+
+def basp_debug_bounds_violations() -> int:
+    """Debug build only: read and clear the count of out-of-bounds accesses
+    the kernels skipped on the current device (synchronises it)."""
+    lib = load_library()
+    if not hasattr(lib, "basp_debug_bounds_violations"):
+        raise RuntimeError("the loaded library is not the bounds-checking build "
+                           "(set BASP_LIBRARY=debug before importing)")
+    n = ctypes.c_ulonglong()
+    _check(lib.basp_debug_bounds_violations(ctypes.byref(n)), "basp_debug_bounds_violations")
+    return n.value
 
 
 def basp_seq2head_qkv(layout, qkv, q_out, k_out, v_out, stream=None):

@@ -1,4 +1,5 @@
-"""Compile ``libbasp.so`` (the C-ABI library) in-tree with nvcc for sm_103a."""
+"""Compile the C-ABI library in-tree with nvcc for sm_103a: ``libbasp.so``
+(release) and ``libbasp_debug.so`` (every kernel access bounds-checked)."""
 from __future__ import annotations
 
 import os
@@ -9,9 +10,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libbasp.so")
+DEBUG_LIB_PATH = os.path.join(PKG, "libbasp_debug.so")
 SOURCES = ["layout.cpp", "relayout.cu"]
-HEADERS = [os.path.join(INCLUDE, "basp.h"), os.path.join(CSRC, "layout_internal.h"),
-           os.path.join(CSRC, "relayout_kernel.cuh")]
+HEADERS = [os.path.join(INCLUDE, "basp.h"), os.path.join(INCLUDE, "basp_debug.h"),
+           os.path.join(CSRC, "layout_internal.h"), os.path.join(CSRC, "relayout_kernel.cuh")]
 
 NVCC_FLAGS = [
     "-O3", "-std=c++17",
@@ -29,25 +31,38 @@ def _nvcc() -> str:
     return "nvcc"
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(path) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     deps = [os.path.join(CSRC, s) for s in SOURCES] + HEADERS
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build_library(force: bool = False, verbose: bool = False) -> str:
-    """Build ``libbasp.so`` next to this file if missing or out of date."""
-    if not force and not _stale():
-        return LIB_PATH
-    tmp = LIB_PATH + ".tmp%d" % os.getpid()
-    cmd = [_nvcc()] + NVCC_FLAGS + ["-I", INCLUDE, "-o", tmp] + \
+def _command(out, extra, verbose):
+    cmd = [_nvcc()] + NVCC_FLAGS + extra + ["-I", INCLUDE, "-o", out] + \
         [os.path.join(CSRC, s) for s in SOURCES]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB_PATH)
+    return cmd
+
+
+def build_library(force: bool = False, verbose: bool = False) -> str:
+    """Build ``libbasp.so`` and ``libbasp_debug.so`` next to this file (the two
+    in parallel) if missing or out of date; return the release library's path."""
+    jobs = []
+    for path, extra in ((LIB_PATH, []), (DEBUG_LIB_PATH, ["-DBASP_CHECK_BOUNDS=1"])):
+        if force or _stale(path):
+            tmp = path + ".tmp%d" % os.getpid()
+            jobs.append((subprocess.Popen(_command(tmp, extra, verbose)), tmp, path))
+    failed = False
+    for proc, tmp, path in jobs:
+        if proc.wait() != 0:
+            failed = True
+        elif not failed:
+            os.replace(tmp, path)
+    if failed:
+        raise subprocess.CalledProcessError(1, "nvcc")
     return LIB_PATH
 
 

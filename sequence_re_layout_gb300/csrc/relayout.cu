@@ -43,10 +43,19 @@
 #include <cstring>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "layout_internal.h"
 #include "relayout_kernel.cuh"
 
 namespace {
+
+// An NVTX range named after the entry point, so profilers show each call
+// (a no-op unless a tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 // ---------------------------------------------------------------------------
 // Host side: stride tables, pass planning, launch.
@@ -123,7 +132,15 @@ struct TensorArg {
     int64_t H;       // heads of this tensor
     int64_t seq_w;   // elements of one token row on the seq-sharded side
                      // (0: H * d; a packed QKV row is (Hq + 2*Hkv) * d)
+    // extents of the buffers around `in` and `out`, in bytes relative to
+    // the pointer (both 0: [0, the tensor's bytes)); bounds-checked builds
+    // test every access against them
+    int64_t in_lo, in_hi, out_lo, out_hi;
 };
+
+// [lo, hi) byte extent -> the vector indices whose whole vector lies inside.
+int64_t vec_lo(int64_t lo, int vec) { return lo >= 0 ? (lo + vec - 1) / vec : -((-lo) / vec); }
+int64_t vec_hi(int64_t hi, int vec) { return hi >= 0 ? hi / vec : -((-hi + vec - 1) / vec); }
 
 int64_t seq_row_elems(const basp_layout &L, const TensorArg &t) {
     return t.seq_w > 0 ? t.seq_w : t.H * L.d;
@@ -200,6 +217,15 @@ basp_status plan(const basp_layout &L, const Pass &pass, const TensorArg *t,
         J.dst_rs = sf ? ds[C_BL] : ds[C_SL];
         J.src = static_cast<const unsigned char *>(t[i].in);
         J.dst = static_cast<unsigned char *>(t[i].out);
+        {
+            const int64_t tb = basp::tensor_bytes(L, t[i].H);
+            const bool di = t[i].in_lo == 0 && t[i].in_hi == 0;
+            const bool dd = t[i].out_lo == 0 && t[i].out_hi == 0;
+            J.src_lo = vec_lo(di ? 0 : t[i].in_lo, vec);
+            J.src_hi = vec_hi(di ? tb : t[i].in_hi, vec);
+            J.dst_lo = vec_lo(dd ? 0 : t[i].out_lo, vec);
+            J.dst_hi = vec_hi(dd ? tb : t[i].out_hi, vec);
+        }
         J.vpr = uint32_t(vpr);
         udiv_magic(J.vpr, &J.vpr_magic, &J.vpr_shift);
         J.vec_per_block = uint32_t(vec_per_block);
@@ -516,11 +542,12 @@ basp_status relayout_qkv(const basp_layout *L, bool to_head, const void *packed,
     for (int i = 0; i < 3; ++i) {
         if (to_head) {
             t[i] = {static_cast<const unsigned char *>(packed) + off[i],
-                    const_cast<void *>(ptrs[i]), H[i], W};
+                    const_cast<void *>(ptrs[i]), H[i], W,
+                    -off[i], packed_bytes - off[i], 0, 0};
         } else {
             t[i] = {ptrs[i],
                     static_cast<unsigned char *>(const_cast<void *>(packed)) + off[i],
-                    H[i], W};
+                    H[i], W, 0, 0, -off[i], packed_bytes - off[i]};
         }
     }
     const int vec = pick_vec(*L, t, 3, nullptr, 0);
@@ -532,6 +559,7 @@ basp_status relayout_qkv(const basp_layout *L, bool to_head, const void *packed,
 extern "C" basp_status basp_seq2head_qkv(const basp_layout *L, const void *qkv,
                                          void *q_out, void *k_out, void *v_out,
                                          cudaStream_t stream) {
+    NvtxRange range("basp_seq2head_qkv");
     return relayout_qkv(L, true, qkv, nullptr, nullptr, nullptr, q_out, k_out,
                         v_out, stream);
 }
@@ -539,6 +567,7 @@ extern "C" basp_status basp_seq2head_qkv(const basp_layout *L, const void *qkv,
 extern "C" basp_status basp_head2seq_qkv(const basp_layout *L, const void *q,
                                          const void *k, const void *v,
                                          void *qkv_out, cudaStream_t stream) {
+    NvtxRange range("basp_head2seq_qkv");
     return relayout_qkv(L, false, qkv_out, q, k, v, nullptr, nullptr, nullptr,
                         stream);
 }
@@ -547,6 +576,7 @@ extern "C" basp_status basp_seq2head(const basp_layout *L, basp_algo algo,
                                      const void *q, const void *k, const void *v,
                                      void *q_out, void *k_out, void *v_out,
                                      void *ws, size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange range("basp_seq2head");
     return relayout(L, algo, true, q, k, v, q_out, k_out, v_out, ws, ws_bytes, stream);
 }
 
@@ -554,6 +584,7 @@ extern "C" basp_status basp_head2seq(const basp_layout *L, basp_algo algo,
                                      const void *o, const void *k, const void *v,
                                      void *o_out, void *k_out, void *v_out,
                                      void *ws, size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange range("basp_head2seq");
     return relayout(L, algo, false, o, k, v, o_out, k_out, v_out, ws, ws_bytes, stream);
 }
 
@@ -562,6 +593,7 @@ extern "C" basp_status basp_seq2head_host(const basp_layout *L, basp_algo algo,
                                           void *q_out, void *k_out, void *v_out,
                                           void *staging, size_t staging_bytes,
                                           void *ws, size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange range("basp_seq2head_host");
     return relayout_host(L, algo, true, q, k, v, q_out, k_out, v_out, staging,
                          staging_bytes, ws, ws_bytes, stream);
 }
@@ -571,6 +603,7 @@ extern "C" basp_status basp_head2seq_host(const basp_layout *L, basp_algo algo,
                                           void *o_out, void *k_out, void *v_out,
                                           void *staging, size_t staging_bytes,
                                           void *ws, size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange range("basp_head2seq_host");
     return relayout_host(L, algo, false, o, k, v, o_out, k_out, v_out, staging,
                          staging_bytes, ws, ws_bytes, stream);
 }
@@ -617,6 +650,7 @@ extern "C" basp_status basp_seq2head_noalloc(const basp_layout *L,
                                              const void *q, const void *k, const void *v,
                                              void *q_out, void *k_out, void *v_out,
                                              cudaStream_t stream) {
+    NvtxRange range("basp_seq2head_noalloc");
     TensorArg t[3];
     int n = 0;
     basp_status st = collect(L, q, k, v, q_out, k_out, v_out, t, &n);
@@ -629,3 +663,17 @@ extern "C" basp_status basp_seq2head_noalloc(const basp_layout *L,
     return relayout(L, BASP_ALGO_THREE_PASS, true, q, k, v, q_out, k_out, v_out,
                     scratch, size_t(BASP_NOALLOC_SCRATCH_BYTES), stream);
 }
+
+#if BASP_CHECK_BOUNDS
+// Debug builds only (libbasp_debug.so, declared in basp_debug.h): read and
+// clear the count of accesses the kernels found outside their buffers.
+extern "C" basp_status basp_debug_bounds_violations(unsigned long long *count) {
+    if (count == nullptr) return BASP_ERR_INVALID_ARG;
+    const unsigned long long zero = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpyFromSymbol(count, g_basp_bounds_violations, sizeof(*count)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_basp_bounds_violations, &zero, sizeof(zero)) != cudaSuccess)
+        return BASP_ERR_CUDA;
+    return BASP_OK;
+}
+#endif

@@ -24,6 +24,9 @@ namespace {
 //   BASP_CTAS_PER_SM           cap on resident CTAs for persistent grids
 //   BASP_PDL                   programmatic dependent launch
 //   BASP_GRID_ALL_TILES        one CTA per tile (1) or a persistent grid (0)
+//   BASP_CHECK_BOUNDS          debug build: every access is checked against
+//                              its buffer's extent; an access outside it is
+//                              counted (g_basp_bounds_violations) and skipped
 #ifndef BASP_THREADS
 #define BASP_THREADS 256
 #endif
@@ -41,6 +44,9 @@ namespace {
 #endif
 #ifndef BASP_PDL
 #define BASP_PDL 1              // programmatic dependent launch (0: plain launch)
+#endif
+#ifndef BASP_CHECK_BOUNDS
+#define BASP_CHECK_BOUNDS 0
 #endif
 #ifndef BASP_GRID_ALL_TILES
 #define BASP_GRID_ALL_TILES 1   // 0: persistent grid (SMs x resident CTAs)
@@ -66,6 +72,8 @@ struct Job {
     uint32_t tiles_per_block;
     uint32_t tile_begin;            // first tile of this job within the launch
     uint32_t inner_fast;            // 1: digit 3 varies fastest across tiles
+    int64_t src_lo, src_hi;         // extent of the source buffer, in vectors
+    int64_t dst_lo, dst_hi;         // from src / dst (checked in debug builds)
 };
 
 struct Params {
@@ -134,6 +142,10 @@ __device__ __forceinline__ void store(unsigned short *p, unsigned short v) {
     asm volatile(BASP_ST ".u16 [%0], %1;" :: "l"(p), "h"(v) : "memory");
 }
 
+#if BASP_CHECK_BOUNDS
+__device__ unsigned long long g_basp_bounds_violations;
+#endif
+
 template <int VEC>
 __global__ void __launch_bounds__(kThreads)
 basp_relayout_kernel(const __grid_constant__ Params p) {
@@ -192,6 +204,25 @@ basp_relayout_kernel(const __grid_constant__ Params p) {
         const W *src = reinterpret_cast<const W *>(J.src) + sb;
         W *dst = reinterpret_cast<W *>(J.dst) + db;
 
+#if BASP_CHECK_BOUNDS
+        (void)src;
+        (void)dst;
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint32_t i = i0 + threadIdx.x + uint32_t(u * kThreads);
+            if (i < i1) {
+                const uint32_t row = (__umulhi(i, J.vpr_magic) + i) >> J.vpr_shift;
+                const uint32_t col = i - row * J.vpr;
+                const int64_t so = sb + int64_t(row) * J.src_rs + col;
+                const int64_t dof = db + int64_t(row) * J.dst_rs + col;
+                if (so < J.src_lo || so >= J.src_hi || dof < J.dst_lo || dof >= J.dst_hi) {
+                    atomicAdd(&g_basp_bounds_violations, 1ull);
+                    continue;
+                }
+                store(reinterpret_cast<W *>(J.dst) + dof,
+                      load_stream(reinterpret_cast<const W *>(J.src) + so));
+            }
+        }
+#else
         W v[kUnroll];
 #if !BASP_RECOMPUTE_DST
         int64_t doff[kUnroll];
@@ -221,6 +252,7 @@ basp_relayout_kernel(const __grid_constant__ Params p) {
 #endif
             }
         }
+#endif  // BASP_CHECK_BOUNDS
     }
 }
 

@@ -20,8 +20,8 @@ def _built():
     build_library()
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(basp_\w+)\s*\(", text)))
 
@@ -33,6 +33,19 @@ def test_every_declared_symbol_is_exported():
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(basp.EXPORTS)
+
+
+def test_debug_library_exports_its_extra_symbol():
+    """libbasp_debug.so exports everything basp.h declares plus what
+    basp_debug.h declares; the release library does not export the latter."""
+    import ctypes
+    from sequence_re_layout_gb300.build import DEBUG_LIB_PATH
+    dbg = ctypes.CDLL(DEBUG_LIB_PATH)
+    extra = declared_functions(HEADER.replace("basp.h", "basp_debug.h"))
+    assert extra == ["basp_debug_bounds_violations"]
+    for n in declared_functions() + extra:
+        assert hasattr(dbg, n), n
+    assert not hasattr(basp.load_library(), extra[0])
 
 
 @pytest.mark.parametrize("args,status", [
