@@ -31,8 +31,8 @@
 // Launch policy (all measured on GB300): one 16 KiB tile per CTA rather than
 // a persistent grid (5-12% faster on HBM: retiring CTAs let new ones start
 // their loads while others drain their stores), except for page-locked host
-// buffers, where a persistent grid keeps more bytes in flight over the host
-// link; programmatic dependent launch, so a kernel's CTAs may be scheduled
+// buffers, where a persistent grid of one CTA per SM moves the most over the
+// host link; programmatic dependent launch, so a kernel's CTAs may be scheduled
 // while the previous kernel on the stream drains (each waits with
 // griddepcontrol.wait before touching memory), hiding the launch gap between
 // back-to-back re-layouts (3-10% per step).
@@ -241,25 +241,33 @@ basp_status plan(const basp_layout &L, const Pass &pass, const TensorArg *t,
     return BASP_OK;
 }
 
+// CTAs per SM of the persistent grid used on page-locked host buffers.  One
+// per SM measured best on GB300 over NVLink-C2C (334 GB/s read+write at the
+// Llama-3.2-1B S=8192 step against 295 with six; the host link's two-way
+// limit measured with the copy engines is about 342).
+constexpr int kHostCtasPerSm = 1;
+
 template <int VEC>
 int grid_for(uint32_t tiles, bool persistent) {
-    // One CTA per tile, or (persistent) every SM filled to its resident-CTA
-    // limit with the CTAs striding over the tiles.  The slot count is cached
-    // per device (a benign race: every thread computes the same numbers).
-    static std::atomic<int> cache[64];
+    // One CTA per tile (device memory), or (persistent, host memory) a grid
+    // of kHostCtasPerSm CTAs per SM striding over the tiles.  The SM count is
+    // cached per device (a benign race: every thread computes the same value).
+    if (BASP_GRID_ALL_TILES && !persistent) return int(tiles);
+    static std::atomic<int> cache[2][64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-    int slots = cache[dev].load(std::memory_order_relaxed);
+    int slots = cache[persistent][dev].load(std::memory_order_relaxed);
     if (slots == 0) {
         int sms = 0, per_sm = 0;
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(
             &per_sm, basp_relayout_kernel<VEC>, kThreads, 0);
-        if (BASP_CTAS_PER_SM > 0 && per_sm > BASP_CTAS_PER_SM) per_sm = BASP_CTAS_PER_SM;
-        slots = (sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
-        cache[dev].store(slots, std::memory_order_relaxed);
+        int cap = persistent ? kHostCtasPerSm : per_sm;
+        if (BASP_CTAS_PER_SM > 0 && cap > BASP_CTAS_PER_SM) cap = BASP_CTAS_PER_SM;
+        if (cap > per_sm) cap = per_sm;
+        slots = (sms > 0 ? sms : 1) * (cap > 0 ? cap : 1);
+        cache[persistent][dev].store(slots, std::memory_order_relaxed);
     }
-    if (BASP_GRID_ALL_TILES && !persistent) return int(tiles);
     return int(tiles < uint32_t(slots) ? tiles : uint32_t(slots));
 }
 
@@ -456,8 +464,8 @@ basp_status relayout_host(const basp_layout *L, basp_algo algo, bool to_head,
     if (staging == nullptr && need > 0) {
         // Direct: every host buffer must be page-locked; the kernels reach it
         // through its device address (the same address under unified
-        // addressing).  A persistent grid keeps more bytes in flight over the
-        // host link than one tile per CTA.
+        // addressing).  A persistent grid of one CTA per SM moves more over
+        // the host link than one tile per CTA.
         const void *hp[6] = {a, k, v, ao, ko, vo};
         const void *dp[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
         for (int x = 0; x < 6; ++x) {

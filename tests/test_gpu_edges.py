@@ -254,3 +254,28 @@ def test_host_entry_points_direct_mode(algo):
         assert e.value.status == basp.BASP_ERR_WORKSPACE
     for name, g, e in zip("qkvo", hout, exp):
         np.testing.assert_array_equal(synth_inputs.bits(g), e, err_msg=name)
+
+
+def test_two_streams_at_once():
+    """Two layouts (BASP and Ulysses) re-laid out concurrently on two streams,
+    each several times back to back: both match the oracle."""
+    B, S, Hq, Hkv, d, N = 2, 2048, 32, 8, 64, 8
+    q, k, v, o = make_inputs(B, S, Hq, Hkv, d, "bf16", 61, kind="bits")
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    layouts = [basp.Layout(B, S, Hq, Hkv, d, N, 4, "bf16"),
+               basp.Layout(B, S, Hq, Hkv, d, N, 8, "bf16")]
+    ins = [t.to(DEV) for t in (q, k, v, o)]
+    outs = [[torch.empty_like(t) for t in ins] for _ in range(2)]
+    torch.cuda.synchronize()
+    for _ in range(5):
+        for L, s, out in zip(layouts, streams, outs):
+            basp.basp_seq2head(L.handle, "fused", ins[0], ins[1], ins[2],
+                               out[0], out[1], out[2], stream=s)
+            basp.basp_head2seq(L.handle, "fused", ins[3], None, None, out[3],
+                               None, None, stream=s)
+    torch.cuda.synchronize()
+    for L, out, K in zip(layouts, outs, (4, 8)):
+        exp = oracle_outputs(q, k, v, o, B, S, Hq, Hkv, d, N, K)
+        for name, g, e in zip("qkvo", out, exp):
+            assert_bits_equal(g, e, "stream K=%d %s" % (K, name))
+        L.close()
