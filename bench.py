@@ -455,7 +455,8 @@ def main_ours(args, dist):
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path)")
-    build_library() if dist.rank == 0 else None
+    if dist.rank == 0:
+        build_library()               # no-op when the library is up to date
     dist.barrier()
     basp.load_library()
     dev = torch.device("cuda", dist.local_rank % torch.cuda.device_count())
@@ -522,6 +523,28 @@ def main_ours(args, dist):
         "gpu_launches": r["launches"],
         "clocks": clocks,
     }
+    if not args.no_extras:
+        # end to end on every rank (replicas): all ranks' bytes over the
+        # slowest rank's time, like `value`
+        ne = max(3, min(args.steps, 50))
+        dist.barrier()
+        e = run_e2e(w, args.layout, args.algo, ne, 3, dev, mode="direct")
+        dist.barrier()
+        es = run_e2e(w, args.layout, args.algo, ne, 3, dev, mode="staged")
+        e_ms, es_ms = dist.max(e["ms_per_step"]), dist.max(es["ms_per_step"])
+        e_bytes, es_bytes = dist.sum(e["step_bytes"]), dist.sum(es["step_bytes"])
+        out["e2e"] = {"value": round(gbs(e_bytes, e_ms), 2),
+                      "unit": "GB/s", "h2d_bytes_per_step": e["bytes_in"] * dist.world,
+                      "d2h_bytes_per_step": e["bytes_out"] * dist.world,
+                      "ms_per_step": round(e_ms, 4),
+                      "api": "basp_seq2head_host + basp_head2seq_host, direct mode "
+                             "(no staging: kernels read and write the pinned host "
+                             "buffers in place)",
+                      "staged": {"value": round(gbs(es_bytes, es_ms), 2),
+                                 "ms_per_step": round(es_ms, 4),
+                                 "api": "basp_seq2head_host + basp_head2seq_host, "
+                                        "staged mode (H2D copy, re-layout, D2H copy)"}}
+        out["gpu_launches"] += 2 * ne * r["launches"] // (2 * args.steps)
     if not args.no_extras and dist.rank == 0:
         other = "ulysses" if args.layout == "basp" else "basp"
         ru = run_device(w, other, args.algo, args.steps, args.warmup, dev,
@@ -565,21 +588,6 @@ def main_ours(args, dist):
             out[alt] = {"value": round(vt, 2), "ms_per_step": round(rt["ms_per_step"], 6),
                         "pct_hbm_peak": round(100 * vt / peak, 2), "note": notes[alt]}
             out["gpu_launches"] += rt["launches"]
-        ne = max(3, min(args.steps, 50))
-        e = run_e2e(w, args.layout, args.algo, ne, 3, dev, mode="direct")
-        es = run_e2e(w, args.layout, args.algo, ne, 3, dev, mode="staged")
-        out["e2e"] = {"value": round(gbs(e["step_bytes"], e["ms_per_step"]), 2),
-                      "unit": "GB/s", "h2d_bytes_per_step": e["bytes_in"],
-                      "d2h_bytes_per_step": e["bytes_out"],
-                      "ms_per_step": round(e["ms_per_step"], 4),
-                      "api": "basp_seq2head_host + basp_head2seq_host, direct mode "
-                             "(no staging: kernels read and write the pinned host "
-                             "buffers in place)",
-                      "staged": {"value": round(gbs(es["step_bytes"], es["ms_per_step"]), 2),
-                                 "ms_per_step": round(es["ms_per_step"], 4),
-                                 "api": "basp_seq2head_host + basp_head2seq_host, "
-                                        "staged mode (H2D copy, re-layout, D2H copy)"}}
-        out["gpu_launches"] += 2 * ne * r["launches"] // (2 * args.steps)
         if dist.world == 1:
             out["cpu_baseline"] = cpu_baseline(w, args.layout, args.cpu_baseline_s)
     if dist.rank == 0:
