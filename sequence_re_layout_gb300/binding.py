@@ -11,9 +11,10 @@ import ctypes
 import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-# BASP_LIBRARY=debug selects the bounds-checking build (libbasp_debug.so)
-LIB_PATH = os.path.join(PKG, "libbasp_debug.so" if os.environ.get("BASP_LIBRARY") == "debug"
-                        else "libbasp.so")
+# BASP_LIBRARY=debug selects the bounds-checking build (libbasp_debug.so);
+# BASP_LIBRARY_PATH names any other build of the same sources explicitly
+LIB_PATH = os.environ.get("BASP_LIBRARY_PATH") or os.path.join(
+    PKG, "libbasp_debug.so" if os.environ.get("BASP_LIBRARY") == "debug" else "libbasp.so")
 
 # enums of basp.h
 BASP_DTYPE_BF16, BASP_DTYPE_FP32, BASP_DTYPE_FP16, BASP_DTYPE_FP8 = 0, 1, 2, 3

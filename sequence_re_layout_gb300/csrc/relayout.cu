@@ -38,6 +38,7 @@
 // back-to-back re-layouts (3-10% per step).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -47,6 +48,12 @@
 
 #include "layout_internal.h"
 #include "relayout_kernel.cuh"
+#ifndef BASP_TMA
+#define BASP_TMA 0     // 1: fused passes use the bulk-copy kernel (comparison build)
+#endif
+#if BASP_TMA
+#include "relayout_tma.cuh"
+#endif
 
 namespace {
 
@@ -293,9 +300,73 @@ basp_status launch_vec(const Params &p, cudaStream_t stream, bool persistent) {
     return cudaGetLastError() == cudaSuccess ? BASP_OK : BASP_ERR_CUDA;
 }
 
+#if BASP_TMA
+// Plan a fused pass for the bulk-copy kernel: tiles of whole rows.  Returns
+// false when a row does not fit the tile or rows are not 16-byte multiples.
+bool plan_rows(const basp_layout &L, const Pass &pass, const TensorArg *t,
+               int n, RowParams *p) {
+    std::memset(p, 0, sizeof(*p));
+    uint64_t tiles = 0;
+    int nj = 0;
+    for (int i = 0; i < n; ++i) {
+        const int64_t row_bytes = (t[i].H / L.K) * L.d * L.esz;
+        const int64_t wseq_bytes = seq_row_elems(L, t[i]) * L.esz;
+        if (row_bytes % 16 || wseq_bytes % 16 || row_bytes > kTmaTileBytes) return false;
+        const bool sf = L.order == BASP_ORDER_SBHD;
+        const int64_t rows = sf ? L.Sk * L.Bg : L.Sk;
+        if (rows == 0) continue;
+        RowJob &J = p->job[nj++];
+        int64_t ss[5], ds[5];
+        strides_of(L, pass.from, row_bytes, wseq_bytes, ss);   // unit: bytes
+        strides_of(L, pass.to, row_bytes, wseq_bytes, ds);
+        for (int k = 0; k < 4; ++k) {
+            J.src_bs[k] = ss[pass.digit[k]];
+            J.dst_bs[k] = ds[pass.digit[k]];
+            J.radix[k] = uint32_t(extent_of(L, pass.digit[k]));
+        }
+        J.src_rs = sf ? ss[C_BL] : ss[C_SL];
+        J.dst_rs = sf ? ds[C_BL] : ds[C_SL];
+        J.src = static_cast<const unsigned char *>(t[i].in);
+        J.dst = static_cast<unsigned char *>(t[i].out);
+        J.row_bytes = uint32_t(row_bytes);
+        J.rows = uint32_t(rows);
+        J.rows_per_tile = uint32_t(std::min<int64_t>(rows, kTmaTileBytes / row_bytes));
+        J.tiles_per_block = (J.rows + J.rows_per_tile - 1) / J.rows_per_tile;
+        J.tile_begin = uint32_t(tiles);
+        tiles += uint64_t(L.G) * L.K * L.K * uint64_t(extent_of(L, C_BL)) * J.tiles_per_block;
+        if (tiles >= (uint64_t(1) << 31)) return false;
+    }
+    p->njobs = nj;
+    p->total_tiles = uint32_t(tiles);
+    return true;
+}
+
+basp_status launch_rows(const RowParams &p, cudaStream_t stream) {
+    if (p.total_tiles == 0) return BASP_OK;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.total_tiles);
+    cfg.blockDim = dim3(32);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, basp_relayout_tma_kernel, p) != cudaSuccess)
+        return BASP_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? BASP_OK : BASP_ERR_CUDA;
+}
+#endif
+
 basp_status run_pass(const basp_layout &L, const Pass &pass,
                      const TensorArg *t, int n, int vec, cudaStream_t stream,
                      bool persistent = false) {
+#if BASP_TMA
+    if (vec == 16 && !persistent && (&pass == &kFusedS2H || &pass == &kFusedH2S)) {
+        RowParams rp;
+        if (plan_rows(L, pass, t, n, &rp)) return launch_rows(rp, stream);
+    }
+#endif
     Params p;
     basp_status st = plan(L, pass, t, n, vec, &p);
     if (st != BASP_OK || p.total_tiles == 0) return st;

@@ -241,3 +241,29 @@ def test_three_pass_elide_workspace_rule():
             basp.basp_seq2head(h, "three_pass_elide", FAKE, None, None, FAKE + nq,
                                None, None, FAKE + nq // 2, nq)
         assert e.value.status == basp.BASP_ERR_ALIASING
+
+
+def test_layouts_from_many_threads():
+    """Layout create / query / destroy from 8 host threads at once, and one
+    shared handle queried concurrently (the handle is immutable)."""
+    import threading
+    shared = basp.Layout(2, 8192, 32, 8, 64, 8, 4, "bf16")
+    errors = []
+
+    def work(seed):
+        try:
+            for i in range(200):
+                K = (1, 2, 4, 8)[(seed + i) % 4]
+                with basp.Layout(8 // K * 2, 64 * K, 8 * K, 8 * K, 16, 8, K) as L:
+                    assert L.info["K"] == K
+                assert basp.basp_layout_query(shared.handle)["peers"] == 3
+        except Exception as e:          # collected and reported below
+            errors.append(e)
+
+    ts = [threading.Thread(target=work, args=(s,)) for s in range(8)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    shared.close()
+    assert not errors, errors[:3]

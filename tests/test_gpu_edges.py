@@ -279,3 +279,43 @@ def test_two_streams_at_once():
         for name, g, e in zip("qkvo", out, exp):
             assert_bits_equal(g, e, "stream K=%d %s" % (K, name))
         L.close()
+
+
+def test_host_threads_share_one_layout():
+    """Four host threads, one shared layout handle, each thread on its own
+    stream with its own buffers, 10 calls each: every result matches."""
+    import threading
+    B, S, Hq, Hkv, d, N, K = 2, 1024, 32, 8, 64, 8, 4
+    q, k, v, o = make_inputs(B, S, Hq, Hkv, d, "bf16", 71, kind="bits")
+    exp = oracle_outputs(q, k, v, o, B, S, Hq, Hkv, d, N, K)
+    L = basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16")
+    ins = [t.to(DEV) for t in (q, k, v, o)]
+    results, errors = {}, []
+
+    def work(idx):
+        try:
+            s = torch.cuda.Stream(device=DEV)
+            outs = [torch.empty_like(t) for t in ins]
+            algo = ALGOS[idx % len(ALGOS)]
+            ws = torch.empty(L.info["workspace_bytes"], dtype=torch.uint8, device=DEV)
+            for _ in range(10):
+                basp.basp_seq2head(L.handle, algo, ins[0], ins[1], ins[2],
+                                   outs[0], outs[1], outs[2], ws, stream=s)
+                basp.basp_head2seq(L.handle, algo, ins[3], None, None, outs[3],
+                                   None, None, ws, stream=s)
+            s.synchronize()
+            results[idx] = outs
+        except Exception as e:          # collected and reported below
+            errors.append(e)
+
+    torch.cuda.synchronize()
+    ts = [threading.Thread(target=work, args=(i,)) for i in range(4)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    L.close()
+    assert not errors, errors[:3]
+    for idx, outs in results.items():
+        for name, g, e in zip("qkvo", outs, exp):
+            assert_bits_equal(g, e, "thread %d %s" % (idx, name))
