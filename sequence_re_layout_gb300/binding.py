@@ -119,6 +119,45 @@ def _ptr(x):
     return x.data_ptr() or None
 
 
+# layout handle -> basp_info dict, so tensor arguments can be checked cheaply
+_INFO = {}
+
+
+def _info(layout):
+    i = _INFO.get(layout)
+    if i is None and layout:
+        i = basp_layout_query(layout)
+    return i
+
+
+def _tptr(x, need, where, name, place):
+    """Address of a buffer argument.  Raw ints pass through unchecked; a tensor
+    must be contiguous, hold at least `need` bytes, and live where the call
+    reads it: "device" (a CUDA tensor, or page-locked host memory, which the
+    kernels reach over the host link) or "host" (CPU memory)."""
+    if x is None or isinstance(x, int):
+        return _ptr(x)
+    if not x.is_contiguous():
+        raise ValueError("%s: %s must be contiguous" % (where, name))
+    if need is not None and x.nbytes < need:
+        raise ValueError("%s: %s holds %d bytes, the layout needs %d"
+                         % (where, name, x.nbytes, need))
+    if place == "device":
+        if not x.is_cuda and not x.is_pinned():
+            raise ValueError("%s: %s must be a CUDA tensor or page-locked host "
+                             "memory" % (where, name))
+    elif x.is_cuda:
+        raise ValueError("%s: %s must be in host memory" % (where, name))
+    return x.data_ptr() or None
+
+
+def _triple(layout, where, names, bufs, place):
+    """Check the (Hq, Hkv, Hkv) buffer triple of one call."""
+    i = _info(layout)
+    need = (i["bytes_q"], i["bytes_kv"], i["bytes_kv"]) if i else (None,) * 3
+    return [_tptr(b, n, where, nm, place) for b, n, nm in zip(bufs, need, names)]
+
+
 def _stream(s):
     if s is None:
         return None
@@ -144,6 +183,7 @@ def basp_layout_create(B, S, Hq, Hkv, d, N, K, dtype="bf16") -> int:
     _check(load_library().basp_layout_create(B, S, Hq, Hkv, d, N, K, code,
                                              ctypes.byref(h)),
            "basp_layout_create")
+    _INFO[h.value] = basp_layout_query(h.value)
     return h.value
 
 
@@ -157,6 +197,7 @@ def basp_layout_create_ex(B, S, Hq, Hkv, d, N, K, dtype="bf16", order="bshd") ->
     h = ctypes.c_void_p()
     _check(load_library().basp_layout_create_ex(ctypes.byref(desc), ctypes.byref(h)),
            "basp_layout_create_ex")
+    _INFO[h.value] = basp_layout_query(h.value)
     return h.value
 
 
@@ -168,6 +209,7 @@ def basp_layout_query(layout: int) -> dict:
 
 
 def basp_layout_destroy(layout: int) -> None:
+    _INFO.pop(layout, None)
     load_library().basp_layout_destroy(layout)
 
 
@@ -187,20 +229,24 @@ def basp_seq2head(layout, algo, q, k, v, q_out, k_out, v_out,
                   workspace=None, workspace_bytes=None, stream=None):
     """seq-sharded -> head-sharded (device buffers); see ``basp.h``."""
     wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    w = "basp_seq2head"
+    a = _triple(layout, w, ("q", "k", "v"), (q, k, v), "device")
+    b = _triple(layout, w, ("q_out", "k_out", "v_out"), (q_out, k_out, v_out), "device")
     _check(load_library().basp_seq2head(
-        layout, _algo(algo), _ptr(q), _ptr(k), _ptr(v), _ptr(q_out),
-        _ptr(k_out), _ptr(v_out), _ptr(workspace), wb, _stream(stream)),
-        "basp_seq2head")
+        layout, _algo(algo), *a, *b,
+        _tptr(workspace, None, w, "workspace", "device"), wb, _stream(stream)), w)
 
 
 def basp_head2seq(layout, algo, o, k, v, o_out, k_out, v_out,
                   workspace=None, workspace_bytes=None, stream=None):
     """head-sharded -> seq-sharded (device buffers); see ``basp.h``."""
     wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    w = "basp_head2seq"
+    a = _triple(layout, w, ("o", "k", "v"), (o, k, v), "device")
+    b = _triple(layout, w, ("o_out", "k_out", "v_out"), (o_out, k_out, v_out), "device")
     _check(load_library().basp_head2seq(
-        layout, _algo(algo), _ptr(o), _ptr(k), _ptr(v), _ptr(o_out),
-        _ptr(k_out), _ptr(v_out), _ptr(workspace), wb, _stream(stream)),
-        "basp_head2seq")
+        layout, _algo(algo), *a, *b,
+        _tptr(workspace, None, w, "workspace", "device"), wb, _stream(stream)), w)
 
 
 def basp_seq2head_host(layout, algo, q, k, v, q_out, k_out, v_out, staging,
@@ -209,10 +255,12 @@ def basp_seq2head_host(layout, algo, q, k, v, q_out, k_out, v_out, staging,
     """Host buffers in and out, device ``staging``; see ``basp.h``."""
     sb = _nbytes(staging) if staging_bytes is None else staging_bytes
     wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    w = "basp_seq2head_host"
+    a = _triple(layout, w, ("q", "k", "v"), (q, k, v), "host")
+    b = _triple(layout, w, ("q_out", "k_out", "v_out"), (q_out, k_out, v_out), "host")
     _check(load_library().basp_seq2head_host(
-        layout, _algo(algo), _ptr(q), _ptr(k), _ptr(v), _ptr(q_out),
-        _ptr(k_out), _ptr(v_out), _ptr(staging), sb, _ptr(workspace), wb,
-        _stream(stream)), "basp_seq2head_host")
+        layout, _algo(algo), *a, *b, _tptr(staging, None, w, "staging", "device"), sb,
+        _tptr(workspace, None, w, "workspace", "device"), wb, _stream(stream)), w)
 
 
 def basp_head2seq_host(layout, algo, o, k, v, o_out, k_out, v_out, staging,
@@ -221,10 +269,12 @@ def basp_head2seq_host(layout, algo, o, k, v, o_out, k_out, v_out, staging,
     """Host buffers in and out, device ``staging``; see ``basp.h``."""
     sb = _nbytes(staging) if staging_bytes is None else staging_bytes
     wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    w = "basp_head2seq_host"
+    a = _triple(layout, w, ("o", "k", "v"), (o, k, v), "host")
+    b = _triple(layout, w, ("o_out", "k_out", "v_out"), (o_out, k_out, v_out), "host")
     _check(load_library().basp_head2seq_host(
-        layout, _algo(algo), _ptr(o), _ptr(k), _ptr(v), _ptr(o_out),
-        _ptr(k_out), _ptr(v_out), _ptr(staging), sb, _ptr(workspace), wb,
-        _stream(stream)), "basp_head2seq_host")
+        layout, _algo(algo), *a, *b, _tptr(staging, None, w, "staging", "device"), sb,
+        _tptr(workspace, None, w, "workspace", "device"), wb, _stream(stream)), w)
 
 
 def basp_debug_bounds_violations() -> int:
@@ -241,16 +291,20 @@ def basp_debug_bounds_violations() -> int:
 
 def basp_seq2head_qkv(layout, qkv, q_out, k_out, v_out, stream=None):
     """Packed seq-sharded QKV -> head-sharded Q, K, V; see ``basp.h``."""
-    _check(load_library().basp_seq2head_qkv(
-        layout, _ptr(qkv), _ptr(q_out), _ptr(k_out), _ptr(v_out),
-        _stream(stream)), "basp_seq2head_qkv")
+    w = "basp_seq2head_qkv"
+    i = _info(layout)
+    p = _tptr(qkv, i["bytes_qkv_packed"] if i else None, w, "qkv", "device")
+    b = _triple(layout, w, ("q_out", "k_out", "v_out"), (q_out, k_out, v_out), "device")
+    _check(load_library().basp_seq2head_qkv(layout, p, *b, _stream(stream)), w)
 
 
 def basp_head2seq_qkv(layout, q, k, v, qkv_out, stream=None):
     """Head-sharded Q, K, V -> packed seq-sharded QKV; see ``basp.h``."""
-    _check(load_library().basp_head2seq_qkv(
-        layout, _ptr(q), _ptr(k), _ptr(v), _ptr(qkv_out), _stream(stream)),
-        "basp_head2seq_qkv")
+    w = "basp_head2seq_qkv"
+    i = _info(layout)
+    a = _triple(layout, w, ("q", "k", "v"), (q, k, v), "device")
+    p = _tptr(qkv_out, i["bytes_qkv_packed"] if i else None, w, "qkv_out", "device")
+    _check(load_library().basp_head2seq_qkv(layout, *a, p, _stream(stream)), w)
 
 
 def basp_seq2head_noalloc(layout, q, k, v, q_out, k_out, v_out, stream=None):
@@ -258,9 +312,10 @@ def basp_seq2head_noalloc(layout, q, k, v, q_out, k_out, v_out, stream=None):
     library's built-in scratch instead of a workspace: for callers that cannot
     allocate device memory.  See ``basp.h`` for the size limit and the rule
     that calls sharing the scratch must not overlap on the GPU."""
-    _check(load_library().basp_seq2head_noalloc(
-        layout, _ptr(q), _ptr(k), _ptr(v), _ptr(q_out), _ptr(k_out),
-        _ptr(v_out), _stream(stream)), "basp_seq2head_noalloc")
+    w = "basp_seq2head_noalloc"
+    a = _triple(layout, w, ("q", "k", "v"), (q, k, v), "device")
+    b = _triple(layout, w, ("q_out", "k_out", "v_out"), (q_out, k_out, v_out), "device")
+    _check(load_library().basp_seq2head_noalloc(layout, *a, *b, _stream(stream)), w)
 
 
 class Layout:

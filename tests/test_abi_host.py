@@ -267,3 +267,23 @@ def test_layouts_from_many_threads():
         t.join()
     shared.close()
     assert not errors, errors[:3]
+
+
+def test_binding_refuses_bad_tensors():
+    """The binding checks tensor arguments before the C call: contiguity,
+    size against the layout, and where the memory lives."""
+    import torch
+    with basp.Layout(2, 64, 8, 4, 16, 4, 2, "bf16") as L:
+        nq = L.info["bytes_q"] // 2
+        q = torch.empty(2 * nq, dtype=torch.bfloat16)[::2]          # strided view
+        with pytest.raises(ValueError, match="contiguous"):
+            basp.basp_seq2head(L.handle, "fused", q, None, None, FAKE, None, None)
+        small = torch.empty(nq - 1, dtype=torch.bfloat16)
+        with pytest.raises(ValueError, match="bytes"):
+            basp.basp_seq2head(L.handle, "fused", small, None, None, FAKE, None, None)
+        pageable = torch.empty(nq, dtype=torch.bfloat16)
+        with pytest.raises(ValueError, match="CUDA tensor or page-locked"):
+            basp.basp_seq2head(L.handle, "fused", pageable, None, None, FAKE, None, None)
+        packed = torch.empty(L.info["bytes_qkv_packed"] // 2 - 1, dtype=torch.bfloat16)
+        with pytest.raises(ValueError, match="bytes"):
+            basp.basp_seq2head_qkv(L.handle, packed, FAKE, FAKE + 2 * nq, FAKE + 4 * nq)
