@@ -70,9 +70,9 @@ typedef enum basp_dtype {
     BASP_DTYPE_FP8 = 3      /* any 1-byte format (e4m3, e5m2, int8), copied as bytes */
 } basp_dtype;
 
-/* Token order inside every rank shard.  The pages fix none; batch-first is the
- * default.  Sequence-first is the [S, B, H, d] activation order of
- * Megatron-style stacks: seq-sharded shards [S/K][Bg][H][d], head-sharded
+/* Token order inside every rank shard.  The BASP review fixes none;
+ * batch-first is the default.  Sequence-first is the [S, B, H, d] activation
+ * order of Megatron-style stacks: seq-sharded shards [S/K][Bg][H][d], head-sharded
  * shards [S][Bg][H/K][d].  With one sequence per group (every BASP layout) the
  * two orders store the same bytes. */
 typedef enum basp_order {
@@ -219,8 +219,8 @@ basp_status basp_head2seq(const basp_layout *layout, basp_algo algo,
  *   basp_head2seq_qkv   the inverse: head-sharded q, k, v (in the backward
  *                       pass, the gradients dQ, dK, dV) -> one packed
  *                       seq-sharded buffer `qkv_out`.
- * All four pointers are required.  The pages describe no projection layout;
- * the head order inside the row is the plainest concatenation.
+ * All four pointers are required.  The BASP review describes no projection
+ * layout; the head order inside the row is the plainest concatenation.
  */
 basp_status basp_seq2head_qkv(const basp_layout *layout, const void *qkv,
                               void *q_out, void *k_out, void *v_out,

@@ -32,8 +32,8 @@ fugumt.com related-papers entry "DeepSpeed Ulysses"):
 The elements are opaque words: pass any numpy dtype (bf16 travels as uint16).
 The result is a bit copy, so tests compare raw bits.
 
-Two variants, neither fixed by the pages (which give no memory order and no
-projection layout):
+Two variants, neither fixed by the BASP review or abstract (which give no
+memory order and no projection layout):
 
 * ``order="sbhd"``: sequence-first shards, the [S, B, H, d] activation order
   of Megatron-style stacks: seq-sharded ``[S/K, Bg, H, d]``, head-sharded

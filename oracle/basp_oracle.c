@@ -34,7 +34,7 @@
  *   head-sharded place; head2seq is the inverse.  Elements are opaque
  *   `esz`-byte words, so the result is a pure bit copy (no rounding).
  *
- * Readings where the pages are silent (each listed in the design notes):
+ * Readings where the BASP review and abstract are silent:
  *   - batch-first [B, S, H, d] order inside a shard (the *_ordered entry
  *     points also take the sequence-first [S, B, H, d] order of Megatron-style
  *     stacks: shards [S/K][Bg][H][d] and [S][Bg][H/K][d]);

@@ -1,6 +1,6 @@
 """CPU checks of the C ABI: the library loads and exports every symbol that
-include/basp.h declares; the layout descriptor applies the pages' rules and
-derives the pages' sizes; compute calls reject bad arguments before anything
+include/basp.h declares; the layout descriptor applies the BASP review's rules
+and derives its sizes; compute calls reject bad arguments before anything
 touches a GPU (no call here reaches a CUDA API)."""
 import os
 import re

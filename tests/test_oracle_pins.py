@@ -1,6 +1,6 @@
-"""Pins for the CPU oracle: what the pages and the mathematics fix.
+"""Pins for the CPU oracle: what the BASP sources and the mathematics fix.
 
-The pages print no worked values for the re-layout, so the oracle is pinned by
+The review and abstract print no worked values for the re-layout, so the oracle is pinned by
 (1) values worked by hand from the definitions, (2) library routines that reach
 the same permutation another way (torch ``permute`` of the logical tensor), (3)
 brute force over every tiny shape, and (4) the invariants the review states:

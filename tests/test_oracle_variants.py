@@ -1,4 +1,4 @@
-"""Pins for the oracle's two variants that the pages leave open: the
+"""Pins for the oracle's two variants that the BASP review leaves open: the
 sequence-first token order ([S, B, H, d], Megatron-style) and the packed QKV
 input (one buffer of Hq + 2*Hkv heads per token row, as a fused QKV projection
 writes it).  Each is checked against torch's permute of the logical tensors,
