@@ -110,16 +110,21 @@ class Dist:
 # ---------------------------------------------------------------------------
 
 def hbm_peak():
+    """The measured HBM copy bandwidth (GB/s) from MEASURED_PEAKS.json, else
+    the fallback.  Accepts the number itself or a nested object holding it
+    ("value", "burst" or "gbs")."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
         v = d.get("hbm_gbs")
+        if v is None and isinstance(d.get("hbm"), dict):
+            v = d["hbm"]
         if isinstance(v, dict):
-            v = v.get("value")
-        if v:
+            v = next((v[k] for k in ("value", "burst", "gbs", "hbm_gbs") if k in v), None)
+        if isinstance(v, (int, float)) and v > 0:
             return float(v), "measured"
-    except (OSError, ValueError):
+    except (OSError, ValueError, AttributeError, TypeError):
         pass
     return FALLBACK_HBM_GBS, "fallback"
 

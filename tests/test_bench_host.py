@@ -95,3 +95,21 @@ def test_reference_arm_under_two_ranks():
     assert len(lines) == 1
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2
+
+
+@pytest.mark.parametrize("content,expect", [
+    ('{"hbm_gbs": 6682.8}', (6682.8, "measured")),
+    ('{"hbm_gbs": {"value": 6500}}', (6500.0, "measured")),
+    ('{"hbm": {"burst": 6600}}', (6600.0, "measured")),
+    ('{"bf16_tflops": 1900}', (bench.FALLBACK_HBM_GBS, "fallback")),
+    ('not json', (bench.FALLBACK_HBM_GBS, "fallback")),
+])
+def test_peak_file_forms(tmp_path, monkeypatch, content, expect):
+    (tmp_path / "MEASURED_PEAKS.json").write_text(content)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.hbm_peak() == expect
+
+
+def test_peak_file_absent(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.hbm_peak() == (bench.FALLBACK_HBM_GBS, "fallback")
