@@ -70,6 +70,9 @@ SMALL = [
     (1, 8, 8, 8, 8, 8, 8),        # one token per rank
     (2, 2056, 24, 8, 128, 8, 4),  # S/K = 514: ragged last tile of each block
     (2, 520, 12, 4, 72, 4, 4),    # vpr = 27 (bf16), not a power of two
+    (8, 256, 32, 16, 16, 64, 8),  # 64 virtual ranks, 8 groups of 8
+    (4, 512, 64, 32, 8, 128, 32), # 128 virtual ranks, 4 groups of 32
+    (2, 96, 48, 48, 8, 48, 24),   # 48 ranks, K = 24 (not a power of two)
 ]
 
 
@@ -90,3 +93,8 @@ def test_small_shapes(shape, dtype):
 def test_full_size_fp8(name, layout):
     """1-byte elements (fp8 activations): the 1-byte word is never split."""
     _check(WORKLOADS[name], "fp8", layout)
+
+
+@pytest.mark.parametrize("layout", ["basp", "ulysses"])
+def test_full_size_fp16(layout):
+    _check(WORKLOADS["llama3.2-1b_B2_S8192"], "fp16", layout)
