@@ -252,7 +252,7 @@ def _alloc_sets(w, K, dtype, n_sets, dev, seed, packed=False):
 
 
 def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
-               packed=False, graph=False):
+               packed=False, graph=False, spread=0):
     """Time `steps` steps of the hot path; returns a dict of timings."""
     import torch
     import sequence_re_layout_gb300 as basp
@@ -349,6 +349,18 @@ def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
 
     s2h_ms = one_kernel("s2h")
     h2s_ms = one_kernel("h2s")
+
+    # spread: the same K-step loop repeated (only reported, never the value)
+    repeats = []
+    for _ in range(spread):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        repeats.append(e0.elapsed_time(e1) / steps)
     passes = {"fused": 1, "three_pass": 3}.get(algo)
     if passes is None:                 # three_pass_elide
         passes = 2 if (info["seqs_per_group"] == 1 or order == "sbhd") else 3
@@ -359,7 +371,8 @@ def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
         "l2_bytes": l2, "s2h_ms_mean": s2h_ms, "h2s_ms_mean": h2s_ms,
         "s2h_bytes": 2 * (info["bytes_q"] + 2 * info["bytes_kv"]),
         "h2s_bytes": 2 * info["bytes_q"],
-        "launches": 2 * launches_per_step * steps,     # step loop + roofline loops
+        "launches": (2 + spread) * launches_per_step * steps,  # step, roofline, spread loops
+        "repeat_ms_per_step": repeats,
         "wall": (soak_t0 if soak_s > 0 else t0, t1),
     }
     del sets, ws
@@ -475,7 +488,7 @@ def main_ours(args, dist):
         raise SystemExit("--qkv-packed runs the fused path only")
     r = run_device(w, args.layout, args.algo, args.steps, args.warmup, dev,
                    soak_s=args.soak_s, order=args.order, packed=args.qkv_packed,
-                   graph=args.graph)
+                   graph=args.graph, spread=0 if args.no_extras else 5)
     sampler.stop()
     dist.barrier()
     t_max = dist.max(r["total_ms"])
@@ -528,6 +541,11 @@ def main_ours(args, dist):
         "gpu_launches": r["launches"],
         "clocks": clocks,
     }
+    if r["repeat_ms_per_step"]:
+        rg = sorted(gbs(r["step_bytes"], ms) for ms in r["repeat_ms_per_step"])
+        out["spread"] = {"repeats": len(rg), "of": "the timed loop, run again after it",
+                         "gbs_min": round(rg[0], 2), "gbs_median": round(statistics.median(rg), 2),
+                         "gbs_max": round(rg[-1], 2)}
     if not args.no_extras:
         # end to end on every rank (replicas): all ranks' bytes over the
         # slowest rank's time, like `value`
@@ -549,7 +567,8 @@ def main_ours(args, dist):
                                  "ms_per_step": round(es_ms, 4),
                                  "api": "basp_seq2head_host + basp_head2seq_host, "
                                         "staged mode (H2D copy, re-layout, D2H copy)"}}
-        out["gpu_launches"] += 2 * ne * r["launches"] // (2 * args.steps)
+        lps = r["launches"] // ((2 + len(r["repeat_ms_per_step"])) * args.steps)
+        out["gpu_launches"] += 2 * ne * lps
     if not args.no_extras and dist.rank == 0:
         other = "ulysses" if args.layout == "basp" else "basp"
         ru = run_device(w, other, args.algo, args.steps, args.warmup, dev,
