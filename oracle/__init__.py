@@ -69,22 +69,35 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def load_from(path):
+    """Load a compiled copy of basp_oracle.c from `path` and declare its entry
+    points (the tests use this to compile deliberately broken copies and
+    check that the pins reject them)."""
+    lib = ctypes.CDLL(path)
+    _declare(lib)
+    return lib
+
+
+def _declare(lib):
+    i64 = ctypes.c_int64
+    for name in ("basp_oracle_seq2head", "basp_oracle_head2seq"):
+        fn = getattr(lib, name)
+        fn.argtypes = [i64] * 7 + [ctypes.c_void_p, ctypes.c_void_p]
+        fn.restype = ctypes.c_int
+    for name in ("basp_oracle_seq2head_ordered", "basp_oracle_head2seq_ordered"):
+        fn = getattr(lib, name)
+        fn.argtypes = [i64] * 7 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+        fn.restype = ctypes.c_int
+    fn = lib.basp_oracle_head_to_seq_index
+    fn.argtypes = [i64] * 7
+    fn.restype = i64
+
+
 def _load():
     global _lib
     if _lib is None:
         lib = ctypes.CDLL(build())
-        i64 = ctypes.c_int64
-        for name in ("basp_oracle_seq2head", "basp_oracle_head2seq"):
-            fn = getattr(lib, name)
-            fn.argtypes = [i64] * 7 + [ctypes.c_void_p, ctypes.c_void_p]
-            fn.restype = ctypes.c_int
-        for name in ("basp_oracle_seq2head_ordered", "basp_oracle_head2seq_ordered"):
-            fn = getattr(lib, name)
-            fn.argtypes = [i64] * 7 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
-            fn.restype = ctypes.c_int
-        fn = lib.basp_oracle_head_to_seq_index
-        fn.argtypes = [i64] * 7
-        fn.restype = i64
+        _declare(lib)
         _lib = lib
     return _lib
 
