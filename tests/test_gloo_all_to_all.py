@@ -28,7 +28,7 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _worker(rank, world, port, shape, result_dir):
+def _worker(rank, world, port, shape, result_dir, order="bshd"):
     B, S, H, d, N, K = shape
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
@@ -41,23 +41,41 @@ def _worker(rank, world, port, shape, result_dir):
         pg = groups[rank // K]
 
         x_all = synth_inputs.normal(B * S * H * d, seed=21, dtype="fp32")
-        x = x_all[rank * P:(rank + 1) * P].view(Bg, Sk, H, d)
+        if order == "bshd":
+            x = x_all[rank * P:(rank + 1) * P].view(Bg, Sk, H, d)
+        else:
+            # sequence-first shard [S/K, Bg, H, d], viewed batch-major for the
+            # same exchange code, then stored back sequence-first
+            x = x_all[rank * P:(rank + 1) * P].view(Sk, Bg, H, d).permute(1, 0, 2, 3)
 
         # seq -> head: send head block j' to member j'; receive token block j
         send = torch.cat([x[:, :, jp * Hk:(jp + 1) * Hk, :].reshape(-1)
                           for jp in range(K)])
         recv = torch.empty_like(send)
         dist.all_to_all_single(recv, send, group=pg)
-        y = recv.view(K, Bg, Sk, Hk, d).permute(1, 0, 2, 3, 4).reshape(-1)
+        y5 = recv.view(K, Bg, Sk, Hk, d)          # [j][bl][sl][hl][e]
+        if order == "bshd":
+            y = y5.permute(1, 0, 2, 3, 4).reshape(-1)
+        else:
+            y = y5.permute(0, 2, 1, 3, 4).reshape(-1)  # [j][sl][bl]: s-major
 
         # head -> seq: send token block j to member j; receive head block j'
-        yv = y.view(Bg, K, Sk, Hk, d)
-        send2 = torch.cat([yv[:, j].reshape(-1) for j in range(K)])
+        if order == "bshd":
+            yv = y.view(Bg, K, Sk, Hk, d)
+            send2 = torch.cat([yv[:, j].reshape(-1) for j in range(K)])
+        else:
+            yv = y.view(K, Sk, Bg, Hk, d)
+            send2 = torch.cat([yv[j].permute(1, 0, 2, 3).reshape(-1) for j in range(K)])
         recv2 = torch.empty_like(send2)
         dist.all_to_all_single(recv2, send2, group=pg)
-        z = recv2.view(K, Bg, Sk, Hk, d).permute(1, 2, 0, 3, 4).reshape(-1)
+        z5 = recv2.view(K, Bg, Sk, Hk, d)         # [j'][bl][sl][hl][e]
+        if order == "bshd":
+            z = z5.permute(1, 2, 0, 3, 4).reshape(-1)
+        else:
+            z = z5.permute(2, 1, 0, 3, 4).reshape(-1)  # [sl][bl][j'][hl][e]
+        x = x_all[rank * P:(rank + 1) * P]
 
-        ref = oracle.seq2head(synth_inputs.bits(x_all), B, S, H, d, N, K)
+        ref = oracle.seq2head(synth_inputs.bits(x_all), B, S, H, d, N, K, order=order)
         ok_y = np.array_equal(synth_inputs.bits(y), ref[rank * P:(rank + 1) * P])
         ok_z = np.array_equal(synth_inputs.bits(z), synth_inputs.bits(x.reshape(-1)))
         with open(os.path.join(result_dir, "r%d" % rank), "w") as f:
@@ -75,10 +93,14 @@ def _worker(rank, world, port, shape, result_dir):
     (2, 16, 8, 4, 4, 4),    # N=4: Ulysses, one group of four
     (4, 8, 4, 2, 4, 2),     # N=4, B=4, two groups holding two sequences each
 ])
-def test_gloo_all_to_all_matches_oracle(shape, tmp_path):
+@pytest.mark.parametrize("order", ["bshd", "sbhd"])
+def test_gloo_all_to_all_matches_oracle(shape, order, tmp_path):
+    """The sequence-first case holds each rank's tokens as [S/K, Bg, H, d]
+    (Megatron-style activations) and must match the oracle's sequence-first
+    shards."""
     oracle.build()
     N = shape[4]
-    mp.spawn(_worker, args=(N, _free_port(), shape, str(tmp_path)), nprocs=N,
+    mp.spawn(_worker, args=(N, _free_port(), shape, str(tmp_path), order), nprocs=N,
              join=True)
     for r in range(N):
         with open(tmp_path / ("r%d" % r)) as f:
