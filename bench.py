@@ -54,7 +54,7 @@ def parse_args():
     p.add_argument("--qkv-packed", action="store_true",
                    help="seq2head reads one packed QKV projection output")
     p.add_argument("--graph", action="store_true",
-                   help="capture each step into a CUDA graph and replay it")
+                   help="capture the timed loop into one CUDA graph and replay it")
     p.add_argument("--soak-s", type=float, default=1.0,
                    help="untimed seconds at full load before the timed region "
                         "(so the clock samples see the loaded GPU)")
@@ -281,25 +281,22 @@ def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
         basp.basp_head2seq(L.handle, algo, ins[3], None, None,
                            outs[3], None, None, ws, stream=stream)
 
+    timed_graph = None
     if graph:
-        # one step per buffer set captured into a CUDA graph (on a side
-        # stream, as capture requires); the graphs replay on the bench stream
-        eager = step
+        # the whole timed loop (`steps` steps, rotating buffers) captured as
+        # one CUDA graph on a side stream, as capture requires, and replayed
+        # once on the bench stream; the programmatic launches become
+        # programmatic edges between the graph's kernel nodes
         for i in range(n_sets):
-            eager(i)                                   # first calls eagerly
+            step(i)                                    # first calls eagerly
         torch.cuda.synchronize(dev)
-        gs = []
         cap = torch.cuda.Stream(dev)
-        for i in range(n_sets):
-            g = torch.cuda.CUDAGraph()
-            stream = cap
-            with torch.cuda.graph(g, stream=cap):
-                eager(i)
-            gs.append(g)
+        timed_graph = torch.cuda.CUDAGraph()
+        stream = cap
+        with torch.cuda.graph(timed_graph, stream=cap):
+            for i in range(steps):
+                step(i)
         stream = torch.cuda.current_stream(dev)
-
-        def step(i):
-            gs[i % n_sets].replay()
 
     for i in range(warmup):
         step(i)
@@ -319,8 +316,11 @@ def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
     # the timed region: `steps` whole steps back to back, events only around
     # the loop (events between launches would serialise them)
     start.record(stream)
-    for i in range(steps):
-        step(i)
+    if timed_graph is not None:
+        timed_graph.replay()
+    else:
+        for i in range(steps):
+            step(i)
     end.record(stream)
     torch.cuda.synchronize(dev)
     t1 = time.time()
