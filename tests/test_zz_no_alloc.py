@@ -19,27 +19,32 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 
 
-@pytest.mark.parametrize("shape", [
+@pytest.mark.parametrize("shape,dtype,order", [
     # (B, S, Hq, Hkv, d, N, K): Llama-3.2-1B heads at S=1024 (24 MiB of
-    # scratch for Q, K, V), BASP and Ulysses
-    (2, 1024, 32, 8, 64, 8, 4),
-    (2, 1024, 32, 8, 64, 8, 8),
+    # scratch for Q, K, V in bf16), BASP and Ulysses; then other element
+    # types and the sequence-first order at sizes that fit the scratch
+    ((2, 1024, 32, 8, 64, 8, 4), "bf16", "bshd"),
+    ((2, 1024, 32, 8, 64, 8, 8), "bf16", "bshd"),
+    ((2, 1024, 32, 8, 64, 8, 8), "bf16", "sbhd"),
+    ((2, 512, 32, 8, 64, 8, 4), "fp32", "bshd"),
+    ((2, 1024, 32, 8, 64, 8, 4), "fp8", "sbhd"),
 ])
-def test_noalloc_matches_seq2head_on_two_calls(shape):
+def test_noalloc_matches_seq2head_on_two_calls(shape, dtype, order):
     B, S, Hq, Hkv, d, N, K = shape
     nq, nkv = B * S * Hq * d, B * S * Hkv * d
-    with basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16") as L:
+    bits = synth_inputs.BITS[synth_inputs.DTYPES[dtype]]
+    with basp.Layout(B, S, Hq, Hkv, d, N, K, dtype, order=order) as L:
         assert 2 * (L.info["bytes_q"] + 2 * L.info["bytes_kv"]) <= basp.BASP_NOALLOC_SCRATCH_BYTES
         for call, seed in enumerate((101, 202)):
-            ins = [synth_inputs.random_bits(n, seed + i, "bf16").to(DEV)
+            ins = [synth_inputs.random_bits(n, seed + i, dtype).to(DEV)
                    for i, n in enumerate((nq, nkv, nkv))]
             want = [torch.empty_like(t) for t in ins]
-            got = [torch.full_like(t, float("nan")) for t in ins]
+            got = [torch.empty_like(t).view(bits).fill_(-1).view(t.dtype) for t in ins]
             basp.basp_seq2head(L.handle, "fused", *ins, *want)
             basp.basp_seq2head_noalloc(L.handle, *ins, *got)
             torch.cuda.synchronize()
             for name, g, w in zip("qkv", got, want):
-                assert torch.equal(g.view(torch.int16), w.view(torch.int16)), \
+                assert torch.equal(g.view(bits), w.view(bits)), \
                     "call %d tensor %s differs" % (call, name)
 
 
