@@ -68,9 +68,10 @@ struct NvtxRange {
 // Host side: stride tables, pass planning, launch.
 // ---------------------------------------------------------------------------
 
-// Strides (in vectors) of the five coordinates for one buffer kind.  `vpr` is
-// the vectors of one row (one rank's head block of one token); `wseq` is the
-// vectors of one whole token row on the seq-sharded side (K * vpr, or the
+// Strides of the five coordinates for one buffer kind, in the unit `vpr` and
+// `wseq` are given in (vectors for the register-copy kernel, bytes for the
+// bulk-copy build).  `vpr` is one row (one rank's head block of one token);
+// `wseq` is one whole token row on the seq-sharded side (K * vpr, or the
 // packed QKV row).  Batch-first shards keep a sequence's tokens together;
 // sequence-first shards interleave the group's sequences token by token.
 void strides_of(const basp_layout &L, BufKind kind, int64_t vpr, int64_t wseq,
