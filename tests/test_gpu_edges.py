@@ -319,3 +319,21 @@ def test_host_threads_share_one_layout():
     for idx, outs in results.items():
         for name, g, e in zip("qkvo", outs, exp):
             assert_bits_equal(g, e, "thread %d %s" % (idx, name))
+
+
+@pytest.mark.parametrize("order", ["bshd", "sbhd"])
+@pytest.mark.parametrize("algo", ALGOS)
+def test_head2seq_with_all_three_slots(algo, order):
+    """head2seq of O, K and V in one call (the backward pass moves dQ, dK, dV
+    this way), every algorithm, both token orders."""
+    B, S, Hq, Hkv, d, N, K = 4, 256, 32, 8, 64, 8, 4       # G = 2, Bg = 2
+    q, k, v, o = make_inputs(B, S, Hq, Hkv, d, "bf16", 83, kind="bits")
+    ins = [t.to(DEV) for t in (o, k, v)]
+    outs = [torch.empty_like(t) for t in ins]
+    with basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16", order=order) as L:
+        ws = torch.empty(L.info["workspace_bytes"], dtype=torch.uint8, device=DEV)
+        basp.basp_head2seq(L.handle, algo, *ins, *outs, ws)
+        torch.cuda.synchronize()
+    for name, t, g, H in zip("okv", (o, k, v), outs, (Hq, Hkv, Hkv)):
+        e = oracle.head2seq(synth_inputs.bits(t), B, S, H, d, N, K, order=order)
+        assert_bits_equal(g, e, "head2seq %s %s %s" % (algo, order, name))
