@@ -117,16 +117,21 @@ def test_side_stream():
             assert_bits_equal(g, e, "side stream %s %s" % (algo, name))
 
 
+@pytest.mark.parametrize("order", ["bshd", "sbhd"])
 @pytest.mark.parametrize("algo", ALGOS)
-def test_host_buffer_entry_points(algo):
+def test_host_buffer_entry_points(algo, order):
     """basp_seq2head_host / basp_head2seq_host: pinned host in, pinned host
     out, device staging owned by the caller."""
-    B, S, Hq, Hkv, d, N, K = 2, 2048, 32, 8, 64, 8, 4
+    B, S, Hq, Hkv, d, N, K = 2, 2048, 32, 8, 64, 8, 8
     q, k, v, o = make_inputs(B, S, Hq, Hkv, d, "bf16", 31)
-    exp = oracle_outputs(q, k, v, o, B, S, Hq, Hkv, d, N, K)
+    bq, bk, bv, bo = (synth_inputs.bits(t) for t in (q, k, v, o))
+    exp = (oracle.seq2head(bq, B, S, Hq, d, N, K, order=order),
+           oracle.seq2head(bk, B, S, Hkv, d, N, K, order=order),
+           oracle.seq2head(bv, B, S, Hkv, d, N, K, order=order),
+           oracle.head2seq(bo, B, S, Hq, d, N, K, order=order))
     hin = [t.pin_memory() for t in (q, k, v, o)]
     hout = [torch.empty_like(t).pin_memory() for t in hin]
-    with basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16") as L:
+    with basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16", order=order) as L:
         staging = torch.empty(L.info["staging_bytes"], dtype=torch.uint8, device=DEV)
         ws = torch.empty(L.info["workspace_bytes"], dtype=torch.uint8, device=DEV)
         st = torch.cuda.current_stream()
