@@ -53,6 +53,8 @@ def parse_args():
                    help="token order inside the shards (batch- or sequence-first)")
     p.add_argument("--qkv-packed", action="store_true",
                    help="seq2head reads one packed QKV projection output")
+    p.add_argument("--dtype", default=None, choices=["bf16", "fp16", "fp32", "fp8"],
+                   help="element type (default: the workload's, bf16)")
     p.add_argument("--graph", action="store_true",
                    help="capture the timed loop into one CUDA graph and replay it")
     p.add_argument("--soak-s", type=float, default=1.0,
@@ -480,6 +482,9 @@ def main_ours(args, dist):
     dev = torch.device("cuda", dist.local_rank % torch.cuda.device_count())
     torch.cuda.set_device(dev)
     w = WORKLOADS[args.config or HEADLINE]
+    if args.dtype:
+        import dataclasses
+        w = dataclasses.replace(w, dtype=args.dtype)
     peak, peak_kind = hbm_peak()
 
     sampler = ClockSampler(dev.index)
