@@ -1,0 +1,47 @@
+"""bench.py on the GPU, briefly: one JSON line with the fields the
+measurement contract names, for the default (extras) run and a short
+sequence-first run."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(*args):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                       capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    return json.loads(lines[0])
+
+
+def test_default_line_has_the_contract_fields():
+    d = _run("--steps", "20", "--warmup", "3", "--soak-s", "0.2", "--cpu-baseline-s", "1")
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
+        assert key in d, key
+    assert d["steps"] == 20 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["value"] > 1000 and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["config"]["workload"] == "llama3.2-1b_B2_S8192"
+    r = d["roofline"]
+    assert r["bound"] == "hbm" and 0 < r["frac"] < 1.5 and r["achieved"] > 0
+    assert set(("value", "unit", "cores", "kind", "sample")) <= set(d["cpu_baseline"])
+    e = d["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert d["gpu_launches"] > 0
+    for alt in ("ulysses", "three_pass", "three_pass_elide", "foil_ulysses_sp_n_over_b"):
+        assert alt in d, alt
+
+
+def test_sequence_first_packed_line():
+    d = _run("--steps", "10", "--warmup", "3", "--soak-s", "0", "--no-extras",
+             "--order", "sbhd", "--qkv-packed", "--config", "llama3.2-3b_B2_S4096")
+    assert d["config"]["order"] == "sbhd" and d["config"]["qkv_packed"] is True
+    assert d["value"] > 1000
