@@ -383,7 +383,7 @@ def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
     return res
 
 
-def run_e2e(w, layout, algo, steps, warmup, dev, mode="staged"):
+def run_e2e(w, layout, algo, steps, warmup, dev, mode="staged", order="bshd"):
     """Same step with the tensors in pinned host memory, inside the timed
     region every step.  mode "staged": basp_seq2head_host / basp_head2seq_host
     copy the inputs to device staging, re-lay out, copy the results back.
@@ -394,7 +394,7 @@ def run_e2e(w, layout, algo, steps, warmup, dev, mode="staged"):
     import sequence_re_layout_gb300 as basp
 
     K = w.K(layout)
-    L = basp.Layout(w.B, w.S, w.Hq, w.Hkv, w.d, w.N, K, w.dtype)
+    L = basp.Layout(w.B, w.S, w.Hq, w.Hkv, w.d, w.N, K, w.dtype, order=order)
     info = L.info
     nq, nkv = w.tensor_elems(w.Hq), w.tensor_elems(w.Hkv)
     hin = [synth_inputs.normal(n, 1234 + i, w.dtype).pin_memory()
@@ -556,9 +556,9 @@ def main_ours(args, dist):
         # slowest rank's time, like `value`
         ne = max(3, min(args.steps, 50))
         dist.barrier()
-        e = run_e2e(w, args.layout, args.algo, ne, 3, dev, mode="direct")
+        e = run_e2e(w, args.layout, args.algo, ne, 3, dev, mode="direct", order=args.order)
         dist.barrier()
-        es = run_e2e(w, args.layout, args.algo, ne, 3, dev, mode="staged")
+        es = run_e2e(w, args.layout, args.algo, ne, 3, dev, mode="staged", order=args.order)
         e_ms, es_ms = dist.max(e["ms_per_step"]), dist.max(es["ms_per_step"])
         e_bytes, es_bytes = dist.sum(e["step_bytes"]), dist.sum(es["step_bytes"])
         out["e2e"] = {"value": round(gbs(e_bytes, e_ms), 2),
