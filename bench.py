@@ -633,7 +633,11 @@ def main_reference(args, dist):
     from sequence_re_layout_gb300.workloads import HEADLINE, WORKLOADS
     oracle.build()
     w = WORKLOADS[args.config or HEADLINE]
+    if args.dtype:
+        import dataclasses
+        w = dataclasses.replace(w, dtype=args.dtype)
     K = w.K(args.layout)
+    o = args.order
     # bound the whole run to about two minutes: shrink S (a multiple of K) so
     # one step takes at most budget / (steps + warmup)
     budget_s = 120.0
@@ -645,10 +649,10 @@ def main_reference(args, dist):
                 for i, n in enumerate(ws)]
 
     def one(S, x):
-        oracle.seq2head(x[0], w.B, S, w.Hq, w.d, w.N, K)
-        oracle.seq2head(x[1], w.B, S, w.Hkv, w.d, w.N, K)
-        oracle.seq2head(x[2], w.B, S, w.Hkv, w.d, w.N, K)
-        oracle.head2seq(x[3], w.B, S, w.Hq, w.d, w.N, K)
+        oracle.seq2head(x[0], w.B, S, w.Hq, w.d, w.N, K, order=o)
+        oracle.seq2head(x[1], w.B, S, w.Hkv, w.d, w.N, K, order=o)
+        oracle.seq2head(x[2], w.B, S, w.Hkv, w.d, w.N, K, order=o)
+        oracle.head2seq(x[3], w.B, S, w.Hq, w.d, w.N, K, order=o)
 
     S = w.S
     probe_S = max(K, (w.S // 16) // K * K)
@@ -677,8 +681,8 @@ def main_reference(args, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (~N(0,1) %s, seeded)" % w.dtype,
         "config": {"workload": w.name, "layout": args.layout, "algo": "oracle",
-                   "B": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
-                   "N": w.N, "K": K},
+                   "order": o, "B": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "d": w.d, "N": w.N, "K": K},
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "GB/s",
