@@ -436,7 +436,7 @@ def run_e2e(w, layout, algo, steps, warmup, dev, mode="staged", order="bshd"):
     return {"ms_per_step": ms, "bytes_in": T, "bytes_out": T, "step_bytes": 2 * T}
 
 
-def cpu_baseline(w, layout, budget_s):
+def cpu_baseline(w, layout, budget_s, order="bshd"):
     """The oracle as it stands (plain C loop, one thread) on the host cores,
     over whole steps of the same workload, repeated until `budget_s`."""
     import oracle
@@ -449,10 +449,10 @@ def cpu_baseline(w, layout, budget_s):
     step_bytes = 2 * (q.nbytes + k.nbytes + v.nbytes + o.nbytes)
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.seq2head(q, w.B, w.S, w.Hq, w.d, w.N, K)
-        oracle.seq2head(k, w.B, w.S, w.Hkv, w.d, w.N, K)
-        oracle.seq2head(v, w.B, w.S, w.Hkv, w.d, w.N, K)
-        oracle.head2seq(o, w.B, w.S, w.Hq, w.d, w.N, K)
+        oracle.seq2head(q, w.B, w.S, w.Hq, w.d, w.N, K, order=order)
+        oracle.seq2head(k, w.B, w.S, w.Hkv, w.d, w.N, K, order=order)
+        oracle.seq2head(v, w.B, w.S, w.Hkv, w.d, w.N, K, order=order)
+        oracle.head2seq(o, w.B, w.S, w.Hq, w.d, w.N, K, order=order)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
@@ -618,7 +618,8 @@ def main_ours(args, dist):
                         "pct_hbm_peak": round(100 * vt / peak, 2), "note": notes[alt]}
             out["gpu_launches"] += rt["launches"]
         if dist.world == 1:
-            out["cpu_baseline"] = cpu_baseline(w, args.layout, args.cpu_baseline_s)
+            out["cpu_baseline"] = cpu_baseline(w, args.layout, args.cpu_baseline_s,
+                                               order=args.order)
     if dist.rank == 0:
         print(json.dumps(out), flush=True)
 
