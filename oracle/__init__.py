@@ -5,11 +5,13 @@ benchmark's CPU-baseline / reference leg may import this package.  The product
 library never imports, links or calls it, and it imports nothing from the
 product package.
 
-Two forms of the same definition live here:
+Three forms of the same definition live here:
 
 * ``seq2head`` / ``head2seq``: the plain element loop in ``basp_oracle.c``
   (source-driven; one ``memcpy`` of ``esz`` bytes per element), reached through
   ctypes.  It is the oracle the parity tests and the CPU baseline use.
+* ``seq2head_threads`` / ``head2seq_threads``: the same element loop with its
+  source rows split over host threads, for timing on every core.
 * ``seq2head_by_slices`` / ``head2seq_by_slices``: the same definition written
   with numpy slicing of the logical tensor ``X[B, S, H, d]``: rebuild ``X``
   from the shards of one layout, cut it into the shards of the other.
@@ -63,7 +65,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB_PATH) or (
             os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
         tmp = _LIB_PATH + ".tmp%d" % os.getpid()
-        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
                         "-o", tmp, _SRC], check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -91,6 +93,12 @@ def _declare(lib):
     fn = lib.basp_oracle_head_to_seq_index
     fn.argtypes = [i64] * 7
     fn.restype = i64
+    for name in ("basp_oracle_seq2head_threads", "basp_oracle_head2seq_threads"):
+        fn = getattr(lib, name, None)
+        if fn is not None:
+            fn.argtypes = [i64] * 7 + [ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_void_p, ctypes.c_void_p]
+            fn.restype = ctypes.c_int
 
 
 def _load():
@@ -152,6 +160,45 @@ def seq2head(x, B, S, H, d, N, K, order="bshd"):
 def head2seq(x, B, S, H, d, N, K, order="bshd"):
     """Inverse of :func:`seq2head`.  Plain C element loop."""
     return _run("basp_oracle_head2seq", x, B, S, H, d, N, K, order)
+
+
+def _run_threads(fn_name, x, B, S, H, d, N, K, order, nthreads):
+    x = np.ascontiguousarray(x)
+    n = B * S * H * d
+    if x.size != n:
+        raise ValueError("input has %d elements, shape needs %d" % (x.size, n))
+    out = np.empty_like(x)
+    if n == 0:
+        return out
+    rc = getattr(_load(), fn_name)(B, S, H, d, N, K, x.itemsize, ORDERS[order],
+                                   int(nthreads), x.ctypes.data, out.ctypes.data)
+    if rc != 0:
+        raise ValueError("shape breaks a divisibility rule (or no threads)")
+    return out
+
+
+def seq2head_threads(x, B, S, H, d, N, K, nthreads, order="bshd"):
+    """:func:`seq2head` on ``nthreads`` host threads: the same element loop,
+    its source rows split into contiguous spans, one per thread (for timing
+    the oracle on every host core; the tests check it against the plain
+    loop)."""
+    return _run_threads("basp_oracle_seq2head_threads", x, B, S, H, d, N, K,
+                        order, nthreads)
+
+
+def head2seq_threads(x, B, S, H, d, N, K, nthreads, order="bshd"):
+    """:func:`head2seq` on ``nthreads`` host threads (see
+    :func:`seq2head_threads`)."""
+    return _run_threads("basp_oracle_head2seq_threads", x, B, S, H, d, N, K,
+                        order, nthreads)
+
+
+def host_cores() -> int:
+    """Cores this process may run on (its CPU affinity set)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
 
 
 def split_packed_qkv(x, Hq, Hkv, d):

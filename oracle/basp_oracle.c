@@ -45,7 +45,9 @@
  * (N % K, B % (N/K), S % K, H % K -- the review's FAQ "What are BASP's main
  * limitations?" requires heads to divide evenly across group members).
  */
+#include <pthread.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 static int shape_ok(int64_t B, int64_t S, int64_t H, int64_t d, int64_t N,
@@ -188,4 +190,111 @@ int64_t basp_oracle_head_to_seq_index(int64_t B, int64_t S, int64_t H,
     const int64_t h  = jp * Hk + hl;
     const int64_t r_in = g * K + j;
     return r_in * P + ((bl * Sk + sl) * H + h) * d + e;
+}
+
+/*
+ * All-core form, for timing the oracle on every host core (the single-thread
+ * walk above stays the reference form; the tests check that both give the
+ * same bytes).  The source rows -- the flattened (r_in, bl, sl) index, one
+ * token of one rank's shard with all H heads -- are cut into `nthreads`
+ * contiguous spans, one per POSIX thread.  Every element has exactly one
+ * destination (the map is a bijection), so the threads write disjoint bytes
+ * and need no locking.  Per element the destination is computed exactly as
+ * in walk_ordered.
+ */
+struct span {
+    int64_t B, S, H, d, N, K, esz;
+    unsigned char *a, *b;
+    int dir, order;
+    int64_t lo, hi;           /* source rows [lo, hi) */
+};
+
+static void *walk_span(void *arg)
+{
+    const struct span *w = (const struct span *)arg;
+    const int64_t K = w->K, H = w->H, d = w->d, esz = w->esz;
+    const int64_t G  = w->N / K;
+    const int64_t Bg = w->B / G;
+    const int64_t Sk = w->S / K;
+    const int64_t Hk = H / K;
+    const int64_t P  = Bg * Sk * H * d;
+    for (int64_t row = w->lo; row < w->hi; ++row) {
+        const int64_t r_in = row / (Bg * Sk);
+        const int64_t bl   = (row / Sk) % Bg;
+        const int64_t sl   = row % Sk;
+        const int64_t g = r_in / K;
+        const int64_t j = r_in % K;
+        const int64_t s = j * Sk + sl;
+        const int64_t t_in  = w->order ? sl * Bg + bl : bl * Sk + sl;
+        const int64_t t_out = w->order ? s * Bg + bl  : bl * w->S + s;
+        for (int64_t h = 0; h < H; ++h) {
+            const int64_t jp = h / Hk;
+            const int64_t hl = h % Hk;
+            const int64_t r_out = g * K + jp;
+            for (int64_t e = 0; e < d; ++e) {
+                const int64_t src = r_in * P + (t_in * H + h) * d + e;
+                const int64_t dst = r_out * P + (t_out * Hk + hl) * d + e;
+                if (w->dir == 0)
+                    memcpy(w->b + dst * esz, w->a + src * esz, (size_t)esz);
+                else
+                    memcpy(w->a + src * esz, w->b + dst * esz, (size_t)esz);
+            }
+        }
+    }
+    return NULL;
+}
+
+static int walk_threads(int64_t B, int64_t S, int64_t H, int64_t d, int64_t N,
+                        int64_t K, int64_t esz, unsigned char *a,
+                        unsigned char *b, int dir, int order, int nthreads)
+{
+    if (!shape_ok(B, S, H, d, N, K, esz) || (order != 0 && order != 1) ||
+        nthreads < 1)
+        return -1;
+    const int64_t rows = N * (B / (N / K)) * (S / K);
+    if (nthreads > 1024) nthreads = 1024;
+    if (rows < nthreads) nthreads = rows > 0 ? (int)rows : 1;
+    struct span *w = (struct span *)malloc(sizeof(struct span) * (size_t)nthreads);
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    unsigned char *running = (unsigned char *)calloc((size_t)nthreads, 1);
+    if (w == NULL || tid == NULL || running == NULL) {
+        free(w);
+        free(tid);
+        free(running);
+        return -1;
+    }
+    int rc = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        const struct span x = {B, S, H, d, N, K, esz, a, b, dir, order,
+                               rows * i / nthreads, rows * (i + 1) / nthreads};
+        w[i] = x;
+        if (i == 0) continue;              /* span 0 runs on this thread */
+        if (pthread_create(&tid[i], NULL, walk_span, &w[i]) == 0)
+            running[i] = 1;
+        else
+            walk_span(&w[i]);              /* no thread: do the span here */
+    }
+    walk_span(&w[0]);
+    for (int i = 1; i < nthreads; ++i)
+        if (running[i] && pthread_join(tid[i], NULL) != 0) rc = -1;
+    free(running);
+    free(w);
+    free(tid);
+    return rc;
+}
+
+int basp_oracle_seq2head_threads(int64_t B, int64_t S, int64_t H, int64_t d,
+                                 int64_t N, int64_t K, int64_t esz, int order,
+                                 int nthreads, const void *in, void *out)
+{
+    return walk_threads(B, S, H, d, N, K, esz, (unsigned char *)in,
+                        (unsigned char *)out, 0, order, nthreads);
+}
+
+int basp_oracle_head2seq_threads(int64_t B, int64_t S, int64_t H, int64_t d,
+                                 int64_t N, int64_t K, int64_t esz, int order,
+                                 int nthreads, const void *in, void *out)
+{
+    return walk_threads(B, S, H, d, N, K, esz, (unsigned char *)out,
+                        (unsigned char *)in, 1, order, nthreads);
 }

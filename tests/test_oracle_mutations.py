@@ -71,7 +71,7 @@ def _compile(text, tmp_path, name):
     src = tmp_path / (name + ".c")
     src.write_text(text)
     so = tmp_path / (name + ".so")
-    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", str(so),
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", str(so),
                     str(src)], check=True)
     return oracle.load_from(str(so))
 
@@ -91,6 +91,10 @@ def test_unmodified_source_passes_every_pin(tmp_path, swap_oracle):
 @pytest.mark.parametrize("what,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
 def test_planted_mistake_is_caught(what, old, new, tmp_path, swap_oracle):
     text = open(SRC).read()
-    assert text.count(old) == 1, "mutation anchor not found: " + old
-    oracle._lib = _compile(text.replace(old, new), tmp_path, "mutant")
+    # the mistakes go into the plain element loop the pins check; the
+    # all-core form after it is pinned against that loop separately
+    cut = text.index("/*\n * All-core form")
+    plain, rest = text[:cut], text[cut:]
+    assert plain.count(old) == 1, "mutation anchor not found: " + old
+    oracle._lib = _compile(plain.replace(old, new) + rest, tmp_path, "mutant")
     assert _pin_failures() > 0, "no pin caught: " + what
