@@ -10,18 +10,24 @@ GB/s counts algorithmic bytes: every element read once and written once,
                     [--layout basp|ulysses] [--algo fused|three_pass]
                     [--impl ours|reference]
 
-Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs an
-independent replica on its own GPU (the path has no cross-GPU step on one
-box); ``value`` is all ranks' bytes over the slowest rank's time.
-``--impl reference`` times the CPU oracle on the host cores instead.
+Prints one JSON line (rank 0).  The default workload is the largest one,
+Llama-3.2-3B-shaped activations at B=2, S=32768.  With N > 1 every rank runs
+an independent replica on its own GPU (the path has no cross-GPU step on one
+box); ``value`` is all ranks' bytes over the slowest rank's time.  Launched
+by torchrun, the ranks come from its environment; ``--gpus N`` alone starts N
+local ranks itself.  ``--impl reference`` times the CPU oracle on the host
+cores instead.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import datetime as _dt
 import hashlib
 import json
+import math
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -37,9 +43,15 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 KERNEL_SOURCE = os.path.join(ROOT, "sequence_re_layout_gb300", "csrc", "relayout_kernel.cuh")
+# A kernel (or the rest of a step) reported above this multiple of the
+# measured copy bandwidth is not believed: the copy peak is itself a
+# read+write of the same bytes, so a permutation can match it, not exceed it
+# by much.
+PLAUSIBLE_FRACTION = 1.15
+CONSISTENT_WITHIN = 0.05
 
 
-def parse_args():
+def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=200)
@@ -60,15 +72,59 @@ def parse_args():
     p.add_argument("--soak-s", type=float, default=1.0,
                    help="untimed seconds at full load before the timed region "
                         "(so the clock samples see the loaded GPU)")
-    p.add_argument("--cpu-baseline-s", type=float, default=10.0)
+    p.add_argument("--window-ms", type=float, default=50.0,
+                   help="shortest window for the per-kernel and steady-step "
+                        "timings (each also spans >= --min-launches launches)")
+    p.add_argument("--min-launches", type=int, default=200)
+    p.add_argument("--cpu-baseline-s", type=float, default=8.0,
+                   help="seconds of the one-thread oracle timing")
+    p.add_argument("--cpu-all-s", type=float, default=4.0,
+                   help="seconds of the all-core oracle timing")
     p.add_argument("--no-extras", action="store_true",
-                   help="skip the Ulysses / three-pass / e2e / CPU legs")
-    return p.parse_args()
+                   help="skip the Ulysses / three-pass / foil / target / e2e / CPU legs")
+    p.add_argument("--no-targets", action="store_true",
+                   help="skip the per-target roofline legs")
+    return p.parse_args(argv)
 
 
 # ---------------------------------------------------------------------------
-# distributed plumbing (replicas only: barrier and max-reduce on the host)
+# ranks: torchrun's environment, or N local processes started here
 # ---------------------------------------------------------------------------
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launch_local_ranks(n: int, argv) -> int:
+    """Run this script as n ranks on this node (RANK / LOCAL_RANK /
+    WORLD_SIZE in each one's environment, rendezvous on 127.0.0.1), as
+    torchrun would.  Returns the first non-zero exit code, else 0; when one
+    rank fails, the others are stopped."""
+    port = _free_port()
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, WORLD_SIZE=str(n), RANK=str(r), LOCAL_RANK=str(r),
+                   LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1",
+                   MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__)] + list(argv),
+                                      env=env))
+    rc = 0
+    live = list(procs)
+    while live:
+        for p in list(live):
+            code = p.poll()
+            if code is None:
+                continue
+            live.remove(p)
+            if code != 0 and rc == 0:
+                rc = code
+                for q in live:
+                    q.terminate()
+        time.sleep(0.05)
+    return rc
+
 
 class Dist:
     def __init__(self):
@@ -231,19 +287,46 @@ def ncu_traffic(workload: str, layout: str, kernel_role: str):
     return None
 
 
+def gbs(nbytes, ms):
+    return nbytes / (ms * 1e-3) / 1e9
+
+
+def check_timings(s2h_bytes, s2h_ms, h2s_bytes, h2s_ms, step_ms, peak):
+    """Cross-check the per-kernel launch times against the step time measured
+    separately: the two kernels' times should add up to the step's (within
+    CONSISTENT_WITHIN), and neither a kernel's own rate nor the rate it
+    implies for the rest of the step may exceed PLAUSIBLE_FRACTION x peak."""
+    total = s2h_ms + h2s_ms
+    rest_after_s2h = step_ms - s2h_ms
+    rest_after_h2s = step_ms - h2s_ms
+    implied_h2s = gbs(h2s_bytes, rest_after_s2h) if rest_after_s2h > 0 else math.inf
+    implied_s2h = gbs(s2h_bytes, rest_after_h2s) if rest_after_h2s > 0 else math.inf
+    rates = [gbs(s2h_bytes, s2h_ms), gbs(h2s_bytes, h2s_ms), implied_h2s, implied_s2h]
+    ratio = total / step_ms
+    return {
+        "s2h_plus_h2s_ms": round(total, 6),
+        "step_ms": round(step_ms, 6),
+        "ratio": round(ratio, 4),
+        "consistent": abs(ratio - 1.0) <= CONSISTENT_WITHIN,
+        "implied_head2seq_gbs": round(implied_h2s, 2) if math.isfinite(implied_h2s) else None,
+        "implied_seq2head_gbs": round(implied_s2h, 2) if math.isfinite(implied_s2h) else None,
+        "plausible": all(math.isfinite(r) and r <= PLAUSIBLE_FRACTION * peak for r in rates),
+    }
+
+
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def _alloc_sets(w, K, dtype, n_sets, dev, seed, packed=False):
+def _alloc_sets(w, dtype, n_sets, dev, seed, packed=False):
     import torch
     import synth_inputs
     nq, nkv = w.tensor_elems(w.Hq), w.tensor_elems(w.Hkv)
-    base = [synth_inputs.normal(n, seed + i, dtype).to(dev)
+    base = [synth_inputs.normal_device(n, seed + i, dtype, dev)
             for i, n in enumerate((nq, nkv, nkv, nq))]
     if packed:
         # ins[0] is the packed QKV buffer; ins[1], ins[2] are unused
-        base[0] = synth_inputs.normal(nq + 2 * nkv, seed + 7, dtype).to(dev)
+        base[0] = synth_inputs.normal_device(nq + 2 * nkv, seed + 7, dtype, dev)
     sets = []
     for s in range(n_sets):
         ins = base if s == 0 else [t.clone() for t in base]
@@ -253,9 +336,10 @@ def _alloc_sets(w, K, dtype, n_sets, dev, seed, packed=False):
     return sets
 
 
-def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
-               packed=False, graph=False, spread=0):
-    """Time `steps` steps of the hot path; returns a dict of timings."""
+def run_device(w, layout, algo, steps, warmup, dev, peak, soak_s=0.0, order="bshd",
+               packed=False, graph=False, spread=0, window_ms=50.0, min_launches=200):
+    """Time `steps` steps of the hot path, then each of the step's two calls
+    alone and a steady window of steps, cross-checked; returns a dict."""
     import torch
     import sequence_re_layout_gb300 as basp
 
@@ -266,22 +350,58 @@ def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
     step_bytes = 2 * T
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     n_sets = min(4096, max(2, -(-4 * l2 // step_bytes) + 1))   # >= 4x L2 per rotation
-    sets = _alloc_sets(w, K, w.dtype, n_sets, dev, 1234, packed)
+    sets = _alloc_sets(w, w.dtype, n_sets, dev, 1234, packed)
     ws = None
     if algo != "fused":
         ws = torch.empty(info["workspace_bytes"], dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # raw addresses, so each call pays only the C ABI's own cost (the binding
+    # checks tensor arguments, raw integers pass through as they are)
+    ptrs = [([t.data_ptr() for t in ins], [t.data_ptr() for t in outs])
+            for ins, outs in sets]
+    wsp = ws.data_ptr() if ws is not None else None
+    wsb = ws.numel() if ws is not None else 0
+    passes = {"fused": 1, "three_pass": 3}.get(algo)
+    if passes is None:                 # three_pass_elide
+        passes = 2 if (info["seqs_per_group"] == 1 or order == "sbhd") else 3
+    count = [0]
+
+    def call(which, i):
+        ins, outs = ptrs[i % n_sets]
+        s = stream.cuda_stream
+        count[0] += passes
+        if which == "s2h" and packed:
+            basp.basp_seq2head_qkv(L.handle, ins[0], outs[0], outs[1], outs[2], stream=s)
+        elif which == "s2h":
+            basp.basp_seq2head(L.handle, algo, ins[0], ins[1], ins[2],
+                               outs[0], outs[1], outs[2], wsp, wsb, stream=s)
+        else:
+            basp.basp_head2seq(L.handle, algo, ins[3], None, None,
+                               outs[3], None, None, wsp, wsb, stream=s)
 
     def step(i):
-        ins, outs = sets[i % n_sets]
-        if packed:
-            basp.basp_seq2head_qkv(L.handle, ins[0], outs[0], outs[1], outs[2],
-                                   stream=stream)
-        else:
-            basp.basp_seq2head(L.handle, algo, ins[0], ins[1], ins[2],
-                               outs[0], outs[1], outs[2], ws, stream=stream)
-        basp.basp_head2seq(L.handle, algo, ins[3], None, None,
-                           outs[3], None, None, ws, stream=stream)
+        call("s2h", i)
+        call("h2s", i)
+
+    def timed(fn, n):
+        """CUDA events around n back-to-back calls on the bench stream (events
+        between launches would break programmatic dependent launch)."""
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for i in range(n):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+
+    def windowed(fn, est_ms):
+        """ms per call over >= min_launches calls and >= window_ms, after a
+        warm-up of that call alone."""
+        timed(fn, 20)
+        n = max(min_launches, int(math.ceil(window_ms / max(est_ms, 1e-4))))
+        return timed(fn, n) / n, n
 
     timed_graph = None
     if graph:
@@ -315,8 +435,8 @@ def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     t0 = time.time()
-    # the timed region: `steps` whole steps back to back, events only around
-    # the loop (events between launches would serialise them)
+    # the timed region: exactly `steps` whole steps back to back, events only
+    # around the loop
     start.record(stream)
     if timed_graph is not None:
         timed_graph.replay()
@@ -327,53 +447,38 @@ def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
     torch.cuda.synchronize(dev)
     t1 = time.time()
     total_ms = start.elapsed_time(end)
+    est_step = total_ms / max(steps, 1)
 
-    # roofline: each kernel's average launch duration, `steps` launches of
-    # that kernel alone back to back on the same stream
-    def one_kernel(which):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(steps):
-            ins, outs = sets[i % n_sets]
-            if which == "s2h" and packed:
-                basp.basp_seq2head_qkv(L.handle, ins[0], outs[0], outs[1], outs[2],
-                                       stream=stream)
-            elif which == "s2h":
-                basp.basp_seq2head(L.handle, algo, ins[0], ins[1], ins[2],
-                                   outs[0], outs[1], outs[2], ws, stream=stream)
-            else:
-                basp.basp_head2seq(L.handle, algo, ins[3], None, None,
-                                   outs[3], None, None, ws, stream=stream)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) / steps
-
-    s2h_ms = one_kernel("s2h")
-    h2s_ms = one_kernel("h2s")
+    # per-call launch times and a steady window of whole steps, measured until
+    # they agree (at most three attempts)
+    attempts = []
+    for _ in range(3):
+        steady_ms, n_steady = windowed(step, est_step)
+        s2h_ms, n_s2h = windowed(lambda i: call("s2h", i), est_step / 2)
+        h2s_ms, n_h2s = windowed(lambda i: call("h2s", i), est_step / 2)
+        chk = check_timings(2 * (info["bytes_q"] + 2 * info["bytes_kv"]), s2h_ms,
+                            2 * info["bytes_q"], h2s_ms, steady_ms, peak)
+        attempts.append((chk, steady_ms, n_steady, s2h_ms, n_s2h, h2s_ms, n_h2s))
+        if chk["consistent"] and chk["plausible"]:
+            break
+    chk, steady_ms, n_steady, s2h_ms, n_s2h, h2s_ms, n_h2s = attempts[-1]
+    chk["attempts"] = len(attempts)
 
     # spread: the same K-step loop repeated (only reported, never the value)
-    repeats = []
-    for _ in range(spread):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(steps):
-            step(i)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        repeats.append(e0.elapsed_time(e1) / steps)
-    passes = {"fused": 1, "three_pass": 3}.get(algo)
-    if passes is None:                 # three_pass_elide
-        passes = 2 if (info["seqs_per_group"] == 1 or order == "sbhd") else 3
+    repeats = [timed(step, steps) / steps for _ in range(spread)]
     launches_per_step = 2 * passes
     res = {
         "total_ms": total_ms, "ms_per_step": total_ms / steps,
         "step_bytes": step_bytes, "info": info, "n_sets": n_sets,
         "l2_bytes": l2, "s2h_ms_mean": s2h_ms, "h2s_ms_mean": h2s_ms,
+        "s2h_launches_timed": n_s2h, "h2s_launches_timed": n_h2s,
+        "steady_ms_per_step": steady_ms, "steady_steps": n_steady,
+        "check": chk,
         "s2h_bytes": 2 * (info["bytes_q"] + 2 * info["bytes_kv"]),
         "h2s_bytes": 2 * info["bytes_q"],
-        "launches": (2 + spread) * launches_per_step * steps,  # step, roofline, spread loops
+        "launches_per_step": launches_per_step,
+        "timed_launches": launches_per_step * steps,
+        "total_launches": count[0],
         "repeat_ms_per_step": repeats,
         "wall": (soak_t0 if soak_s > 0 else t0, t1),
     }
@@ -381,6 +486,37 @@ def run_device(w, layout, algo, steps, warmup, dev, soak_s=0.0, order="bshd",
     L.close()
     torch.cuda.empty_cache()
     return res
+
+
+def kernel_roofline(nbytes, ms, peak, traffic, plausible):
+    """One call's roofline entry: algorithmic bytes over its mean launch time."""
+    a = gbs(nbytes, ms)
+    if not plausible:
+        return {"achieved": None, "frac": None, "traffic": traffic,
+                "algorithmic_bytes_per_launch": nbytes, "launch_ms_mean": round(ms, 6),
+                "note": "withheld: the launch times and the step time disagree "
+                        "beyond what the copy peak allows"}
+    return {"achieved": round(a, 2), "frac": round(a / peak, 4), "traffic": traffic,
+            "algorithmic_bytes_per_launch": nbytes, "launch_ms_mean": round(ms, 6)}
+
+
+def leg_summary(w, layout, r, peak, order="bshd", packed=False, algo="fused"):
+    """Both directions' rooflines, the steady step and the cross-check of one
+    (workload, layout) run."""
+    traffic = {"s2h": None, "h2s": None}
+    if order == "bshd" and not packed:
+        traffic["s2h"] = ncu_traffic(w.name, layout, "seq2head_qkv_" + algo)
+        traffic["h2s"] = ncu_traffic(w.name, layout, "head2seq_o_" + algo)
+    ok = r["check"]["plausible"]
+    s2h = kernel_roofline(r["s2h_bytes"], r["s2h_ms_mean"], peak, traffic["s2h"], ok)
+    h2s = kernel_roofline(r["h2s_bytes"], r["h2s_ms_mean"], peak, traffic["h2s"], ok)
+    steady = gbs(r["step_bytes"], r["steady_ms_per_step"])
+    return {"workload": w.name, "layout": layout, "K": r["info"]["K"],
+            "seq2head": s2h, "head2seq": h2s,
+            "steady_step": {"gbs": round(steady, 2), "frac": round(steady / peak, 4),
+                            "ms": round(r["steady_ms_per_step"], 6),
+                            "steps": r["steady_steps"]},
+            "check": r["check"]}
 
 
 def run_e2e(w, layout, algo, steps, warmup, dev, mode="staged", order="bshd"):
@@ -397,10 +533,15 @@ def run_e2e(w, layout, algo, steps, warmup, dev, mode="staged", order="bshd"):
     L = basp.Layout(w.B, w.S, w.Hq, w.Hkv, w.d, w.N, K, w.dtype, order=order)
     info = L.info
     nq, nkv = w.tensor_elems(w.Hq), w.tensor_elems(w.Hkv)
-    hin = [synth_inputs.normal(n, 1234 + i, w.dtype).pin_memory()
-           for i, n in enumerate((nq, nkv, nkv, nq))]
+    hin = []
+    for i, n in enumerate((nq, nkv, nkv, nq)):
+        h = torch.empty(n, dtype=synth_inputs.DTYPES[w.dtype]).pin_memory()
+        h.copy_(synth_inputs.normal_device(n, 1234 + i, w.dtype, dev))
+        hin.append(h)
     hout = [torch.empty_like(t).pin_memory() for t in hin]
-    staging = torch.empty(info["staging_bytes"], dtype=torch.uint8, device=dev)
+    staging = None
+    if mode == "staged":
+        staging = torch.empty(info["staging_bytes"], dtype=torch.uint8, device=dev)
     ws = None
     if algo != "fused":
         ws = torch.empty(info["workspace_bytes"], dtype=torch.uint8, device=dev)
@@ -432,46 +573,81 @@ def run_e2e(w, layout, algo, steps, warmup, dev, mode="staged", order="bshd"):
     torch.cuda.synchronize(dev)
     ms = start.elapsed_time(end) / steps
     T = sum(t.numel() * t.element_size() for t in hin)
+    del staging, ws, hin, hout
     L.close()
-    return {"ms_per_step": ms, "bytes_in": T, "bytes_out": T, "step_bytes": 2 * T}
+    torch.cuda.empty_cache()
+    return {"ms_per_step": ms, "bytes_in": T, "bytes_out": T, "step_bytes": 2 * T,
+            "launches": (warmup + steps) * 2}
 
 
-def cpu_baseline(w, layout, budget_s, order="bshd"):
-    """The oracle as it stands (plain C loop, one thread) on the host cores,
-    over whole steps of the same workload, repeated until `budget_s`."""
+def _oracle_step(w, K, x, order, nthreads=None):
+    """One step of the oracle: Q, K, V seq2head and O head2seq."""
     import oracle
+    hs = (w.Hq, w.Hkv, w.Hkv, w.Hq)
+    for i, (a, H) in enumerate(zip(x, hs)):
+        fwd = i < 3
+        if nthreads is None:
+            f = oracle.seq2head if fwd else oracle.head2seq
+            f(a, w.B, w.S, H, w.d, w.N, K, order=order)
+        else:
+            f = oracle.seq2head_threads if fwd else oracle.head2seq_threads
+            f(a, w.B, w.S, H, w.d, w.N, K, nthreads, order=order)
+
+
+def _oracle_inputs(w, on_gpu=False):
+    """The step's four tensors as raw bits on the host, drawn by the CPU
+    generator, or (on_gpu, which is much faster at full size) by the GPU's."""
+    import torch
     import synth_inputs
-    oracle.build()
-    K = w.K(layout)
-    nq, nkv = w.tensor_elems(w.Hq), w.tensor_elems(w.Hkv)
-    q, k, v, o = (synth_inputs.bits(synth_inputs.normal(n, 1234 + i, w.dtype))
-                  for i, n in enumerate((nq, nkv, nkv, nq)))
-    step_bytes = 2 * (q.nbytes + k.nbytes + v.nbytes + o.nbytes)
+    sizes = [w.B * w.S * h * w.d for h in (w.Hq, w.Hkv, w.Hkv, w.Hq)]
+    if on_gpu:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        return [synth_inputs.bits(synth_inputs.normal_device(n, 1234 + i, w.dtype, dev).cpu())
+                for i, n in enumerate(sizes)]
+    return [synth_inputs.bits(synth_inputs.normal(n, 1234 + i, w.dtype))
+            for i, n in enumerate(sizes)]
+
+
+def _time_oracle(w, K, x, order, budget_s, nthreads):
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.seq2head(q, w.B, w.S, w.Hq, w.d, w.N, K, order=order)
-        oracle.seq2head(k, w.B, w.S, w.Hkv, w.d, w.N, K, order=order)
-        oracle.seq2head(v, w.B, w.S, w.Hkv, w.d, w.N, K, order=order)
-        oracle.head2seq(o, w.B, w.S, w.Hq, w.d, w.N, K, order=order)
+        _oracle_step(w, K, x, order, nthreads)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
-            break
-    return {"value": round(step_bytes * reps / el / 1e9, 3), "unit": "GB/s",
-            "cores": 1, "kind": "oracle",
-            "sample": "%d whole steps of %s (%s, Q/K/V seq2head + O head2seq), "
-                      "%.1f s" % (reps, w.name, layout, el)}
+            return reps, el
 
 
-def gbs(nbytes, ms):
-    return nbytes / (ms * 1e-3) / 1e9
+def cpu_baseline(w, layout, budget_1, budget_all, order="bshd"):
+    """The oracle as it stands on the host cores, over whole steps of the same
+    workload: the plain loop on one thread for about `budget_1` s, then the
+    all-core form on every core this process may use for about `budget_all` s."""
+    import oracle
+    oracle.build()
+    K = w.K(layout)
+    x = _oracle_inputs(w, on_gpu=True)
+    step_bytes = 2 * sum(a.nbytes for a in x)
+    cores = oracle.host_cores()
+    r1, e1 = _time_oracle(w, K, x, order, budget_1, None)
+    ra, ea = _time_oracle(w, K, x, order, budget_all, cores)
+    v1 = step_bytes * r1 / e1 / 1e9
+    va = step_bytes * ra / ea / 1e9
+    return {"value": round(va, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "%d whole steps of %s (%s, Q/K/V seq2head + O head2seq) on %d "
+                      "threads, %.1f s" % (ra, w.name, layout, cores, ea),
+            "threads_all": {"value": round(va, 3), "threads": cores, "steps": ra,
+                            "seconds": round(ea, 2)},
+            "threads_1": {"value": round(v1, 3), "threads": 1, "steps": r1,
+                          "seconds": round(e1, 2)},
+            "host_cores": cores}
 
 
 def main_ours(args, dist):
     import torch
     import sequence_re_layout_gb300 as basp
     from sequence_re_layout_gb300.build import build_library
-    from sequence_re_layout_gb300.workloads import HEADLINE, WORKLOADS
+    from sequence_re_layout_gb300.workloads import (HEADLINE, TARGETS,
+                                                    TARGET_FRACTION, WORKLOADS, Workload)
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path)")
@@ -483,29 +659,28 @@ def main_ours(args, dist):
     torch.cuda.set_device(dev)
     w = WORKLOADS[args.config or HEADLINE]
     if args.dtype:
-        import dataclasses
         w = dataclasses.replace(w, dtype=args.dtype)
     peak, peak_kind = hbm_peak()
+    kw = dict(window_ms=args.window_ms, min_launches=args.min_launches)
 
     sampler = ClockSampler(dev.index)
     dist.barrier()
     if args.qkv_packed and args.algo != "fused":
         raise SystemExit("--qkv-packed runs the fused path only")
-    r = run_device(w, args.layout, args.algo, args.steps, args.warmup, dev,
+    r = run_device(w, args.layout, args.algo, args.steps, args.warmup, dev, peak,
                    soak_s=args.soak_s, order=args.order, packed=args.qkv_packed,
-                   graph=args.graph, spread=0 if args.no_extras else 5)
+                   graph=args.graph, spread=0 if args.no_extras else 5, **kw)
     sampler.stop()
     dist.barrier()
     t_max = dist.max(r["total_ms"])
     total_bytes = dist.sum(r["step_bytes"] * args.steps)
     value = total_bytes / (t_max * 1e-3) / 1e9
     clocks = sampler.summary(*r["wall"])
+    launches_total = r["total_launches"]
 
     info = r["info"]
-    s2h_gbs = gbs(r["s2h_bytes"], r["s2h_ms_mean"])
-    traffic = None
-    if args.order == "bshd" and not args.qkv_packed:
-        traffic = ncu_traffic(w.name, args.layout, "seq2head_qkv_" + args.algo)
+    head = leg_summary(w, args.layout, r, peak, args.order, args.qkv_packed, args.algo)
+    s2h = head["seq2head"]
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
@@ -526,24 +701,25 @@ def main_ours(args, dist):
         },
         "pct_hbm_peak": round(100 * value / dist.world / peak, 2),
         "pct_hbm_nominal": round(100 * value / dist.world / NOMINAL_HBM_GBS, 2),
-        "roofline": {
+        "roofline": dict({
             "bound": "hbm", "kernel": "basp_relayout_kernel<16> (seq2head Q,K,V)",
-            "achieved": round(s2h_gbs, 2), "peak": peak, "unit": "GB/s",
-            "frac": round(s2h_gbs / peak, 4), "traffic": traffic,
-            "algorithmic_bytes_per_launch": r["s2h_bytes"],
-            "launch_ms_mean": round(r["s2h_ms_mean"], 6),
-            "launch_timing": "CUDA events around %d back-to-back launches of "
-                             "this kernel alone on the bench stream" % args.steps,
-            "peak_kind": "of %s" % peak_kind,
-        },
-        "head2seq": {"achieved_gbs": round(gbs(r["h2s_bytes"], r["h2s_ms_mean"]), 2),
-                     "launch_ms_mean": round(r["h2s_ms_mean"], 6)},
+            "peak": peak, "unit": "GB/s",
+            "launch_timing": "CUDA events around %d back-to-back launches of this "
+                             "kernel alone on the bench stream, after 20 untimed "
+                             "ones" % r["s2h_launches_timed"],
+            "peak_kind": "of %s" % peak_kind}, **s2h),
+        "head2seq": dict(head["head2seq"], launches_timed=r["h2s_launches_timed"]),
+        "steady": dict(head["steady_step"],
+                       note="the same step over a window of >= %g ms, after the "
+                            "timed region; `value` is the timed region alone"
+                            % args.window_ms),
+        "timing_check": head["check"],
         "analytic": {"peers_per_rank": info["peers"],
                      "bytes_per_peer_q": info["bytes_per_peer_q"],
                      "bytes_per_peer_kv": info["bytes_per_peer_kv"],
                      "tokens_per_rank": info["tokens_per_rank"],
                      "foil_tokens_per_rank": info["foil_tokens_per_rank"]},
-        "gpu_launches": r["launches"],
+        "gpu_launches": r["timed_launches"],
         "clocks": clocks,
     }
     if r["repeat_ms_per_step"]:
@@ -572,37 +748,42 @@ def main_ours(args, dist):
                                  "ms_per_step": round(es_ms, 4),
                                  "api": "basp_seq2head_host + basp_head2seq_host, "
                                         "staged mode (H2D copy, re-layout, D2H copy)"}}
-        lps = r["launches"] // ((2 + len(r["repeat_ms_per_step"])) * args.steps)
-        out["gpu_launches"] += 2 * ne * lps
+        launches_total += e["launches"] * r["launches_per_step"] // 2
+        launches_total += es["launches"] * r["launches_per_step"] // 2
     if not args.no_extras and dist.rank == 0:
         other = "ulysses" if args.layout == "basp" else "basp"
-        ru = run_device(w, other, args.algo, args.steps, args.warmup, dev,
-                        order=args.order, packed=args.qkv_packed)
+        ru = run_device(w, other, args.algo, args.steps, args.warmup, dev, peak,
+                        order=args.order, packed=args.qkv_packed, **kw)
+        lu = leg_summary(w, other, ru, peak, args.order, args.qkv_packed, args.algo)
         vu = gbs(ru["step_bytes"] * args.steps, ru["total_ms"])
         ou = ru["info"]
         out[other] = {"value": round(vu, 2), "ms_per_step": round(ru["ms_per_step"], 6),
                       "K": ou["K"], "pct_hbm_peak": round(100 * vu / peak, 2),
                       "peers_per_rank": ou["peers"],
                       "bytes_per_peer_q": ou["bytes_per_peer_q"],
-                      "seq2head_gbs": round(gbs(ru["s2h_bytes"], ru["s2h_ms_mean"]), 2)}
+                      "seq2head": lu["seq2head"], "head2seq": lu["head2seq"],
+                      "steady": lu["steady_step"], "timing_check": lu["check"]}
+        launches_total += ru["total_launches"]
+        legs = {(w.name, args.layout): head, (w.name, other): lu}
         if args.layout == "basp" and w.N % w.B == 0:
             # the review's "trivial alternative" (Strengths, Table I): Ulysses
             # with SP = N/B, every group of K = N/B ranks holding all B
             # sequences -- B*B*S/N tokens per rank, B times BASP's bytes
-            from sequence_re_layout_gb300.workloads import Workload
             wf = Workload(w.name + "_foil", w.B * w.B, w.S, w.Hq, w.Hkv, w.d,
                           w.N, w.N // w.B, w.dtype)
-            rf = run_device(wf, "basp", args.algo, args.steps, args.warmup, dev,
-                            order=args.order)
+            rf = run_device(wf, "basp", args.algo, args.steps, args.warmup, dev, peak,
+                            order=args.order, **kw)
             out["foil_ulysses_sp_n_over_b"] = {
                 "tokens_per_rank": rf["info"]["tokens_per_rank"],
                 "basp_tokens_per_rank": info["tokens_per_rank"],
                 "bytes_per_step": rf["step_bytes"],
                 "ms_per_step": round(rf["ms_per_step"], 6),
                 "value": round(gbs(rf["step_bytes"] * args.steps, rf["total_ms"]), 2),
-                "time_vs_basp": round(rf["ms_per_step"] / (r["total_ms"] / args.steps), 3)}
-            out["gpu_launches"] += rf["launches"]
-        out["gpu_launches"] += ru["launches"]
+                "time_vs_basp": round(rf["ms_per_step"] / (r["total_ms"] / args.steps), 3),
+                "steady_time_vs_basp": round(rf["steady_ms_per_step"] /
+                                             r["steady_ms_per_step"], 3),
+                "timing_check": rf["check"]}
+            launches_total += rf["total_launches"]
         alts = [a for a in ("fused", "three_pass", "three_pass_elide") if a != args.algo]
         notes = {"three_pass": "same algorithmic bytes; the three passes move them 3x",
                  "three_pass_elide": "identity pass skipped when the receive chunks "
@@ -611,70 +792,83 @@ def main_ours(args, dist):
                                         args.order == "sbhd" else "no"),
                  "fused": "one pass"}
         for alt in alts:
-            rt = run_device(w, args.layout, alt, args.steps, args.warmup, dev,
-                            order=args.order)
+            rt = run_device(w, args.layout, alt, args.steps, args.warmup, dev, peak,
+                            order=args.order, **kw)
             vt = gbs(rt["step_bytes"] * args.steps, rt["total_ms"])
             out[alt] = {"value": round(vt, 2), "ms_per_step": round(rt["ms_per_step"], 6),
                         "pct_hbm_peak": round(100 * vt / peak, 2), "note": notes[alt]}
-            out["gpu_launches"] += rt["launches"]
+            launches_total += rt["total_launches"]
+        if (not args.no_targets and args.algo == "fused" and args.order == "bshd"
+                and not args.qkv_packed and not args.dtype):
+            # every long-sequence target shape, both layouts, both directions
+            for name in TARGETS:
+                for lay in ("basp", "ulysses"):
+                    if (name, lay) in legs:
+                        continue
+                    wt = WORKLOADS[name]
+                    rt = run_device(wt, lay, "fused", args.steps, args.warmup, dev, peak, **kw)
+                    legs[(name, lay)] = leg_summary(wt, lay, rt, peak)
+                    launches_total += rt["total_launches"]
+            tl = []
+            for name in TARGETS:
+                for lay in ("basp", "ulysses"):
+                    leg = dict(legs[(name, lay)])
+                    fr = [leg[k]["frac"] for k in ("seq2head", "head2seq")]
+                    leg["meets_bar"] = all(f is not None and f >= TARGET_FRACTION for f in fr)
+                    tl.append(leg)
+            out["targets"] = {"bar": TARGET_FRACTION, "peak": peak,
+                              "peak_kind": "of %s" % peak_kind,
+                              "all_meet_bar": all(l["meets_bar"] for l in tl),
+                              "legs": tl}
         if dist.world == 1:
             out["cpu_baseline"] = cpu_baseline(w, args.layout, args.cpu_baseline_s,
-                                               order=args.order)
+                                               args.cpu_all_s, order=args.order)
+    out["gpu_launches_total"] = launches_total
     if dist.rank == 0:
         print(json.dumps(out), flush=True)
 
 
 def main_reference(args, dist):
     """The reference arm: the CPU oracle, as it stands, timed on the host
-    cores over bounded samples of the same workload (rank 0 only)."""
+    cores (its all-core form, every core this process may use) over bounded
+    samples of the same workload (rank 0 only)."""
     if dist.rank != 0:
         return
     import oracle
-    import synth_inputs
     from sequence_re_layout_gb300.workloads import HEADLINE, WORKLOADS
     oracle.build()
     w = WORKLOADS[args.config or HEADLINE]
     if args.dtype:
-        import dataclasses
         w = dataclasses.replace(w, dtype=args.dtype)
     K = w.K(args.layout)
     o = args.order
-    # bound the whole run to about two minutes: shrink S (a multiple of K) so
-    # one step takes at most budget / (steps + warmup)
+    cores = oracle.host_cores()
+    # bound the whole run to about two minutes: if one full-size step would
+    # take longer than budget / (steps + warmup), shrink S (a multiple of K).
+    # Inputs are drawn on the CPU: nothing on this arm touches the GPU.
     budget_s = 120.0
-    nq, nkv = w.tensor_elems(w.Hq), w.tensor_elems(w.Hkv)
-
-    def make(S):
-        ws = [w.B * S * h * w.d for h in (w.Hq, w.Hkv, w.Hkv, w.Hq)]
-        return [synth_inputs.bits(synth_inputs.normal(n, 1234 + i, w.dtype))
-                for i, n in enumerate(ws)]
-
-    def one(S, x):
-        oracle.seq2head(x[0], w.B, S, w.Hq, w.d, w.N, K, order=o)
-        oracle.seq2head(x[1], w.B, S, w.Hkv, w.d, w.N, K, order=o)
-        oracle.seq2head(x[2], w.B, S, w.Hkv, w.d, w.N, K, order=o)
-        oracle.head2seq(x[3], w.B, S, w.Hq, w.d, w.N, K, order=o)
-
-    S = w.S
     probe_S = max(K, (w.S // 16) // K * K)
-    xp = make(probe_S)
+    wp = dataclasses.replace(w, S=probe_S)
+    xp = _oracle_inputs(wp)
     t0 = time.perf_counter()
-    one(probe_S, xp)
+    _oracle_step(wp, K, xp, o, cores)
     per_token = (time.perf_counter() - t0) / probe_S
     per_step_budget = budget_s / max(1, args.steps + args.warmup)
+    S = w.S
     if per_token * w.S > per_step_budget:
         S = max(K, int(per_step_budget / per_token) // K * K)
-    x = make(S)
+    ws = dataclasses.replace(w, S=S)
+    x = _oracle_inputs(ws)
     for _ in range(args.warmup):
-        one(S, x)
+        _oracle_step(ws, K, x, o, cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        one(S, x)
+        _oracle_step(ws, K, x, o, cores)
     el = time.perf_counter() - t0
     step_bytes = 2 * sum(a.nbytes for a in x)
     value = step_bytes * args.steps / el / 1e9
-    sample = ("%s at S=%d of %d (same B, heads, d, N, K), %d steps, %.1f s"
-              % (w.name, S, w.S, args.steps, el))
+    sample = ("%s at S=%d of %d (same B, heads, d, N, K), %d steps on %d threads, %.1f s"
+              % (w.name, S, w.S, args.steps, cores, el))
     out = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3),
         "unit": "GB/s", "n_gpus": dist.world, "steps": args.steps,
@@ -684,7 +878,7 @@ def main_reference(args, dist):
         "config": {"workload": w.name, "layout": args.layout, "algo": "oracle",
                    "order": o, "B": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv,
                    "d": w.d, "N": w.N, "K": K},
-        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1,
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "GB/s",
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -692,8 +886,16 @@ def main_reference(args, dist):
     print(json.dumps(out), flush=True)
 
 
-def main():
-    args = parse_args()
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else argv
+    args = parse_args(argv)
+    env_world = os.environ.get("WORLD_SIZE")
+    if env_world is None and args.gpus > 1:
+        sys.exit(launch_local_ranks(args.gpus, argv))
+    if env_world is not None and int(env_world) != args.gpus:
+        print("bench.py: --gpus %d but WORLD_SIZE=%s; they must agree"
+              % (args.gpus, env_world), file=sys.stderr)
+        sys.exit(2)
     dist = Dist()
     try:
         if args.impl == "reference":

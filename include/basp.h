@@ -279,7 +279,11 @@ basp_status basp_head2seq_host(const basp_layout *layout, basp_algo algo,
  * The first call on each device looks up the array's device address on that
  * device (cudaGetSymbolAddress, with that device current), which may load the
  * library's device code there; make that first call before any stream
- * capture.  Every call shares the one array: calls whose kernels can overlap
+ * capture.  The address is kept per CUDA context, keyed by the driver's
+ * context ID: after a device reset the device has a new context, and the next
+ * call looks the address up again instead of using the old one.  (As for any
+ * CUDA library, nothing of it may be in use on the device while it is
+ * reset.)  Every call shares the one array: calls whose kernels can overlap
  * on the GPU (different streams, or several host threads) race on it and
  * corrupt each other's results, so keep them on one stream.  Each call
  * writes every scratch byte before reading it, so nothing has to start at

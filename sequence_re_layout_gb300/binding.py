@@ -130,11 +130,17 @@ def _info(layout):
     return i
 
 
+def _current_device() -> int:
+    import torch
+    return torch.cuda.current_device()
+
+
 def _tptr(x, need, where, name, place):
     """Address of a buffer argument.  Raw ints pass through unchecked; a tensor
     must be contiguous, hold at least `need` bytes, and live where the call
-    reads it: "device" (a CUDA tensor, or page-locked host memory, which the
-    kernels reach over the host link) or "host" (CPU memory)."""
+    reads it: "device" (a CUDA tensor on the current device, or page-locked
+    host memory, which the kernels reach over the host link) or "host" (CPU
+    memory)."""
     if x is None or isinstance(x, int):
         return _ptr(x)
     if not x.is_contiguous():
@@ -143,7 +149,16 @@ def _tptr(x, need, where, name, place):
         raise ValueError("%s: %s holds %d bytes, the layout needs %d"
                          % (where, name, x.nbytes, need))
     if place == "device":
-        if not x.is_cuda and not x.is_pinned():
+        if x.is_cuda:
+            # the library launches on the current device (and takes its
+            # built-in scratch there), so a tensor on another GPU would be
+            # reached across devices: refuse it
+            cur = _current_device()
+            if x.device.index != cur:
+                raise ValueError("%s: %s is on cuda:%s but the current device is "
+                                 "cuda:%d; make its device current first"
+                                 % (where, name, x.device.index, cur))
+        elif not x.is_pinned():
             raise ValueError("%s: %s must be a CUDA tensor or page-locked host "
                              "memory" % (where, name))
     elif x.is_cuda:

@@ -13,7 +13,8 @@ LIB_PATH = os.path.join(PKG, "libbasp.so")
 DEBUG_LIB_PATH = os.path.join(PKG, "libbasp_debug.so")
 SOURCES = ["layout.cpp", "relayout.cu"]
 HEADERS = [os.path.join(INCLUDE, "basp.h"), os.path.join(INCLUDE, "basp_debug.h"),
-           os.path.join(CSRC, "layout_internal.h"), os.path.join(CSRC, "relayout_kernel.cuh")]
+           os.path.join(CSRC, "layout_internal.h"), os.path.join(CSRC, "relayout_kernel.cuh"),
+           os.path.join(CSRC, "scratch_cache.h")]
 
 NVCC_FLAGS = [
     "-O3", "-std=c++17",

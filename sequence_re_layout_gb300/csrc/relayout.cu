@@ -35,7 +35,10 @@
 // host link; programmatic dependent launch, so a kernel's CTAs may be scheduled
 // while the previous kernel on the stream drains (each waits with
 // griddepcontrol.wait before touching memory), hiding the launch gap between
-// back-to-back re-layouts (3-10% per step).
+// back-to-back re-layouts (3-10% per step); and an L2 prefetch of each CTA's
+// tile before that wait, which overlaps the first DRAM reads of a launch with
+// the previous one's tail (+1% per step at S=32768, +18% at S=1024).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -48,12 +51,7 @@
 
 #include "layout_internal.h"
 #include "relayout_kernel.cuh"
-#ifndef BASP_TMA
-#define BASP_TMA 0     // 1: fused passes use the bulk-copy kernel (comparison build)
-#endif
-#if BASP_TMA
-#include "relayout_tma.cuh"
-#endif
+#include "scratch_cache.h"
 
 namespace {
 
@@ -69,8 +67,7 @@ struct NvtxRange {
 // ---------------------------------------------------------------------------
 
 // Strides of the five coordinates for one buffer kind, in the unit `vpr` and
-// `wseq` are given in (vectors for the register-copy kernel, bytes for the
-// bulk-copy build).  `vpr` is one row (one rank's head block of one token);
+// `wseq` are given in (vectors of the launch's width).  `vpr` is one row (one rank's head block of one token);
 // `wseq` is one whole token row on the seq-sharded side (K * vpr, or the
 // packed QKV row).  Batch-first shards keep a sequence's tokens together;
 // sequence-first shards interleave the group's sequences token by token.
@@ -255,36 +252,47 @@ basp_status plan(const basp_layout &L, const Pass &pass, const TensorArg *t,
 // limit measured with the copy engines is about 342).
 constexpr int kHostCtasPerSm = 1;
 
+// CTA slots of one wave on the current device: SMs x resident CTAs of the
+// kernel (persistent: at most kHostCtasPerSm per SM).  Cached per device (a
+// benign race: every thread computes the same value).
 template <int VEC>
-int grid_for(uint32_t tiles, bool persistent) {
-    // One CTA per tile (device memory), or (persistent, host memory) a grid
-    // of kHostCtasPerSm CTAs per SM striding over the tiles.  The SM count is
-    // cached per device (a benign race: every thread computes the same value).
-    if (BASP_GRID_ALL_TILES && !persistent) return int(tiles);
+uint32_t wave_slots(bool persistent) {
     static std::atomic<int> cache[2][64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
     int slots = cache[persistent][dev].load(std::memory_order_relaxed);
     if (slots == 0) {
         int sms = 0, per_sm = 0;
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, basp_relayout_kernel<VEC>, kThreads, 0);
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &per_sm, basp_relayout_kernel<VEC>, kThreads, 0) != cudaSuccess) {
+            cudaGetLastError();           // clear the error this probe caused
+            return 1;
+        }
         int cap = persistent ? kHostCtasPerSm : per_sm;
         if (BASP_CTAS_PER_SM > 0 && cap > BASP_CTAS_PER_SM) cap = BASP_CTAS_PER_SM;
         if (cap > per_sm) cap = per_sm;
         slots = (sms > 0 ? sms : 1) * (cap > 0 ? cap : 1);
         cache[persistent][dev].store(slots, std::memory_order_relaxed);
     }
-    return int(tiles < uint32_t(slots) ? tiles : uint32_t(slots));
+    return uint32_t(slots);
 }
 
+// One CTA per tile (device memory), or (persistent, host memory) a grid of
+// kHostCtasPerSm CTAs per SM striding over the tiles.  The CTAs of a
+// device-memory grid prefetch their tile into L2 first (BASP_PREFETCH: all of
+// them, or those of the first wave); host memory is never prefetched.
 template <int VEC>
-basp_status launch_vec(const Params &p, cudaStream_t stream, bool persistent) {
-    const int grid = grid_for<VEC>(p.total_tiles, persistent);
+basp_status launch_vec(Params p, cudaStream_t stream, bool persistent) {
+    const uint32_t slots = wave_slots<VEC>(persistent);
+    uint32_t grid = p.total_tiles < slots ? p.total_tiles : slots;
+    if (BASP_GRID_ALL_TILES && !persistent) grid = p.total_tiles;
+    p.prefetch_ctas = 0;
+    if (!persistent && BASP_PREFETCH == 1) p.prefetch_ctas = slots;
+    if (!persistent && BASP_PREFETCH == 2) p.prefetch_ctas = p.total_tiles;
 #if BASP_PDL
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(grid));
+    cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -293,81 +301,22 @@ basp_status launch_vec(const Params &p, cudaStream_t stream, bool persistent) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, basp_relayout_kernel<VEC>, p) != cudaSuccess)
+    // the launch's own status: an error the caller left pending is not ours
+    if (cudaLaunchKernelEx(&cfg, basp_relayout_kernel<VEC>, p) != cudaSuccess) {
+        cudaGetLastError();               // clear the error this launch set
         return BASP_ERR_CUDA;
-#else
-    basp_relayout_kernel<VEC><<<grid, kThreads, 0, stream>>>(p);
-#endif
-    return cudaGetLastError() == cudaSuccess ? BASP_OK : BASP_ERR_CUDA;
-}
-
-#if BASP_TMA
-// Plan a fused pass for the bulk-copy kernel: tiles of whole rows.  Returns
-// false when a row does not fit the tile or rows are not 16-byte multiples.
-bool plan_rows(const basp_layout &L, const Pass &pass, const TensorArg *t,
-               int n, RowParams *p) {
-    std::memset(p, 0, sizeof(*p));
-    uint64_t tiles = 0;
-    int nj = 0;
-    for (int i = 0; i < n; ++i) {
-        const int64_t row_bytes = (t[i].H / L.K) * L.d * L.esz;
-        const int64_t wseq_bytes = seq_row_elems(L, t[i]) * L.esz;
-        if (row_bytes % 16 || wseq_bytes % 16 || row_bytes > kTmaTileBytes) return false;
-        const bool sf = L.order == BASP_ORDER_SBHD;
-        const int64_t rows = sf ? L.Sk * L.Bg : L.Sk;
-        if (rows == 0) continue;
-        RowJob &J = p->job[nj++];
-        int64_t ss[5], ds[5];
-        strides_of(L, pass.from, row_bytes, wseq_bytes, ss);   // unit: bytes
-        strides_of(L, pass.to, row_bytes, wseq_bytes, ds);
-        for (int k = 0; k < 4; ++k) {
-            J.src_bs[k] = ss[pass.digit[k]];
-            J.dst_bs[k] = ds[pass.digit[k]];
-            J.radix[k] = uint32_t(extent_of(L, pass.digit[k]));
-        }
-        J.src_rs = sf ? ss[C_BL] : ss[C_SL];
-        J.dst_rs = sf ? ds[C_BL] : ds[C_SL];
-        J.src = static_cast<const unsigned char *>(t[i].in);
-        J.dst = static_cast<unsigned char *>(t[i].out);
-        J.row_bytes = uint32_t(row_bytes);
-        J.rows = uint32_t(rows);
-        J.rows_per_tile = uint32_t(std::min<int64_t>(rows, kTmaTileBytes / row_bytes));
-        J.tiles_per_block = (J.rows + J.rows_per_tile - 1) / J.rows_per_tile;
-        J.tile_begin = uint32_t(tiles);
-        tiles += uint64_t(L.G) * L.K * L.K * uint64_t(extent_of(L, C_BL)) * J.tiles_per_block;
-        if (tiles >= (uint64_t(1) << 31)) return false;
     }
-    p->njobs = nj;
-    p->total_tiles = uint32_t(tiles);
-    return true;
-}
-
-basp_status launch_rows(const RowParams &p, cudaStream_t stream) {
-    if (p.total_tiles == 0) return BASP_OK;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.total_tiles);
-    cfg.blockDim = dim3(32);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, basp_relayout_tma_kernel, p) != cudaSuccess)
-        return BASP_ERR_CUDA;
+    return BASP_OK;
+#else
+    cudaGetLastError();                   // start from a clean error state
+    basp_relayout_kernel<VEC><<<grid, kThreads, 0, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? BASP_OK : BASP_ERR_CUDA;
-}
 #endif
+}
 
 basp_status run_pass(const basp_layout &L, const Pass &pass,
                      const TensorArg *t, int n, int vec, cudaStream_t stream,
                      bool persistent = false) {
-#if BASP_TMA
-    if (vec == 16 && !persistent && (&pass == &kFusedS2H || &pass == &kFusedH2S)) {
-        RowParams rp;
-        if (plan_rows(L, pass, t, n, &rp)) return launch_rows(rp, stream);
-    }
-#endif
     Params p;
     basp_status st = plan(L, pass, t, n, vec, &p);
     if (st != BASP_OK || p.total_tiles == 0) return st;
@@ -698,30 +647,64 @@ static __device__ __align__(256) unsigned char
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_setup_mutex;
-std::atomic<void *> g_noalloc_addr[kMaxDevices];
-
-// The array's device address on the current device.  In host code the name
+// The array's device address in the current context.  In host code the name
 // g_noalloc_scratch is only a host-side stand-in, so the address is looked up
-// once per device, with that device current.
-basp_status noalloc_scratch(void **out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return BASP_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return BASP_ERR_INVALID_ARG;
-    void *p = g_noalloc_addr[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
-        std::lock_guard<std::mutex> lock(g_noalloc_setup_mutex);
-        p = g_noalloc_addr[dev].load(std::memory_order_acquire);
-        if (p == nullptr) {
-            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess ||
-                p == nullptr)
-                return BASP_ERR_CUDA;
-            g_noalloc_addr[dev].store(p, std::memory_order_release);
+// with cudaGetSymbolAddress, with the caller's device current, once per
+// context: the first call on a device does the lookup (which may load the
+// library's device code there) and later calls reuse it.  The cache
+// (scratch_cache.h) is keyed by the driver's context ID, which is never reused
+// within a process, so a device reset (after which the device code is loaded
+// afresh, perhaps at another address) leads to a new lookup rather than a
+// stale address.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+struct DriverCtxQuery {
+    CtxGetCurrentFn get_current = nullptr;
+    CtxGetIdFn get_id = nullptr;
+};
+
+const DriverCtxQuery &driver_ctx_query() {
+    static const DriverCtxQuery q = [] {
+        DriverCtxQuery r;
+        void *f = nullptr, *g = nullptr;
+        cudaDriverEntryPointQueryResult qr1, qr2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000,
+                                             cudaEnableDefault, &qr1) == cudaSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &g, 12000,
+                                             cudaEnableDefault, &qr2) == cudaSuccess &&
+            qr1 == cudaDriverEntryPointSuccess && qr2 == cudaDriverEntryPointSuccess) {
+            r.get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+            r.get_id = reinterpret_cast<CtxGetIdFn>(g);
+        } else {
+            cudaGetLastError();
         }
-    }
-    *out = p;
-    return BASP_OK;
+        return r;
+    }();
+    return q;
+}
+
+// ID of the context current on this thread, or 0 if none is (or the driver
+// cannot say).
+unsigned long long current_ctx_id() {
+    const DriverCtxQuery &q = driver_ctx_query();
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (q.get_current == nullptr || q.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+        return 0;
+    if (q.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+basp::ScratchAddressCache<64> g_noalloc_cache;
+
+basp_status noalloc_scratch(void **out) {
+    const bool ok = g_noalloc_cache.get(current_ctx_id, [](void **p) {
+        if (cudaGetSymbolAddress(p, g_noalloc_scratch) == cudaSuccess) return true;
+        cudaGetLastError();               // clear the error this lookup set
+        return false;
+    }, out);
+    return ok ? BASP_OK : BASP_ERR_CUDA;
 }
 
 }  // namespace

@@ -8,6 +8,9 @@
 // job's stride tables, and vector i of the block sits in row i / vpr,
 // column i % vpr.  Loads are non-coherent and skip L1; stores are
 // evict-first.  Every thread issues its kUnroll loads before its stores.
+// Every CTA first prefetches its tile's source lines into L2; the ones
+// resident before the previous kernel on the stream has finished do so while
+// it drains, before they wait for it.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -24,6 +27,9 @@ namespace {
 //   BASP_CTAS_PER_SM           cap on resident CTAs for persistent grids
 //   BASP_PDL                   programmatic dependent launch
 //   BASP_GRID_ALL_TILES        one CTA per tile (1) or a persistent grid (0)
+//   BASP_PREFETCH              L2 prefetch of the first tile before the wait
+//                              for the previous kernel: 0 none, 1 the CTAs of
+//                              the first wave, 2 every CTA
 //   BASP_CHECK_BOUNDS          debug build: every access is checked against
 //                              its buffer's extent; an access outside it is
 //                              counted (g_basp_bounds_violations) and skipped
@@ -50,6 +56,9 @@ namespace {
 #endif
 #ifndef BASP_GRID_ALL_TILES
 #define BASP_GRID_ALL_TILES 1   // 0: persistent grid (SMs x resident CTAs)
+#endif
+#ifndef BASP_PREFETCH
+#define BASP_PREFETCH 2
 #endif
 constexpr int kThreads = BASP_THREADS;   // threads per CTA
 constexpr int kUnroll = BASP_UNROLL;     // vectors in flight per thread
@@ -80,6 +89,7 @@ struct Params {
     Job job[kMaxJobs];
     int njobs;
     uint32_t total_tiles;
+    uint32_t prefetch_ctas;   // CTAs below this index prefetch their first tile
 };
 
 template <int VEC> struct Word;
@@ -146,114 +156,168 @@ __device__ __forceinline__ void store(unsigned short *p, unsigned short v) {
 __device__ unsigned long long g_basp_bounds_violations;
 #endif
 
+// One tile located: its job, the source and destination bases of its block
+// (in vectors), and its vector range [i0, i1) within the block.
+struct Tile {
+    const Job *J;
+    int64_t sb, db;
+    uint32_t i0, i1;
+};
+
+// tile -> (job, block digits, tile within block).  Tiles run either block by
+// block (inner_fast = 0) or with the innermost block digit varying fastest,
+// so that consecutive tiles fill neighbouring row segments.
+__device__ __forceinline__ Tile locate(const Params &p, uint32_t t) {
+    int jb = 0;
+    if (p.njobs > 1 && t >= p.job[1].tile_begin) jb = 1;
+    if (p.njobs > 2 && t >= p.job[2].tile_begin) jb = 2;
+    const Job &J = p.job[jb];
+    uint32_t lt = t - J.tile_begin;
+    uint32_t tb, q;
+    int64_t sb = 0, db = 0;
+    if (J.inner_fast) {
+        q = lt / J.radix[3];
+        const uint32_t d3 = lt - q * J.radix[3];
+        sb += int64_t(d3) * J.src_bs[3];
+        db += int64_t(d3) * J.dst_bs[3];
+        lt = q;
+        q = lt / J.tiles_per_block;
+        tb = lt - q * J.tiles_per_block;
+        lt = q;
+    } else {
+        q = lt / J.tiles_per_block;
+        tb = lt - q * J.tiles_per_block;
+        lt = q;
+        q = lt / J.radix[3];
+        const uint32_t d3 = lt - q * J.radix[3];
+        sb += int64_t(d3) * J.src_bs[3];
+        db += int64_t(d3) * J.dst_bs[3];
+        lt = q;
+    }
+#pragma unroll
+    for (int k = 2; k >= 1; --k) {
+        q = lt / J.radix[k];
+        const uint32_t dgt = lt - q * J.radix[k];
+        sb += int64_t(dgt) * J.src_bs[k];
+        db += int64_t(dgt) * J.dst_bs[k];
+        lt = q;
+    }
+    sb += int64_t(lt) * J.src_bs[0];
+    db += int64_t(lt) * J.dst_bs[0];
+    Tile T;
+    T.J = &J;
+    T.sb = sb;
+    T.db = db;
+    T.i0 = tb * uint32_t(kTileVec);
+    T.i1 = min(T.i0 + uint32_t(kTileVec), J.vec_per_block);
+    return T;
+}
+
+// Row and column of vector i of a block: row = i / vpr by the job's
+// multiply-high constants, col = i - row * vpr.
+__device__ __forceinline__ uint32_t row_of(const Job &J, uint32_t i) {
+    return (__umulhi(i, J.vpr_magic) + i) >> J.vpr_shift;
+}
+
+// Ask L2 for the lines the tile will read.  A prefetch hands no value to the
+// thread, so it may run before the previous kernel on the stream has finished:
+// L2 is where every SM's accesses meet, so a line that kernel writes later is
+// updated there, and the loads after griddepcontrol.wait see its final value.
+template <int VEC>
+__device__ __forceinline__ void prefetch_tile(const Tile &T) {
+    using W = typename Word<VEC>::T;
+    const Job &J = *T.J;
+    const W *src = reinterpret_cast<const W *>(J.src) + T.sb;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const uint32_t i = T.i0 + threadIdx.x + uint32_t(u * kThreads);
+        if (i < T.i1) {
+            const uint32_t row = row_of(J, i);
+            const int64_t so = int64_t(row) * J.src_rs + (i - row * J.vpr);
+#if BASP_CHECK_BOUNDS
+            if (T.sb + so < J.src_lo || T.sb + so >= J.src_hi) continue;
+#endif
+            asm volatile("prefetch.global.L2 [%0];" :: "l"(src + so));
+        }
+    }
+}
+
+template <int VEC>
+__device__ __forceinline__ void copy_tile(const Tile &T) {
+    using W = typename Word<VEC>::T;
+    const Job &J = *T.J;
+    const W *src = reinterpret_cast<const W *>(J.src) + T.sb;
+    W *dst = reinterpret_cast<W *>(J.dst) + T.db;
+#if BASP_CHECK_BOUNDS
+    for (int u = 0; u < kUnroll; ++u) {
+        const uint32_t i = T.i0 + threadIdx.x + uint32_t(u * kThreads);
+        if (i < T.i1) {
+            const uint32_t row = row_of(J, i);
+            const uint32_t col = i - row * J.vpr;
+            const int64_t so = T.sb + int64_t(row) * J.src_rs + col;
+            const int64_t dof = T.db + int64_t(row) * J.dst_rs + col;
+            if (so < J.src_lo || so >= J.src_hi || dof < J.dst_lo || dof >= J.dst_hi) {
+                atomicAdd(&g_basp_bounds_violations, 1ull);
+                continue;
+            }
+            store(reinterpret_cast<W *>(J.dst) + dof,
+                  load_stream(reinterpret_cast<const W *>(J.src) + so));
+        }
+    }
+    (void)src;
+    (void)dst;
+#else
+    W v[kUnroll];
+#if !BASP_RECOMPUTE_DST
+    int64_t doff[kUnroll];
+#endif
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const uint32_t i = T.i0 + threadIdx.x + uint32_t(u * kThreads);
+        if (i < T.i1) {
+            const uint32_t row = row_of(J, i);
+            const uint32_t col = i - row * J.vpr;
+            v[u] = load_stream(src + (int64_t(row) * J.src_rs + col));
+#if !BASP_RECOMPUTE_DST
+            doff[u] = int64_t(row) * J.dst_rs + col;
+#endif
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const uint32_t i = T.i0 + threadIdx.x + uint32_t(u * kThreads);
+        if (i < T.i1) {
+#if BASP_RECOMPUTE_DST
+            const uint32_t row = row_of(J, i);
+            store(dst + (int64_t(row) * J.dst_rs + (i - row * J.vpr)), v[u]);
+#else
+            store(dst + doff[u], v[u]);
+#endif
+        }
+    }
+#endif  // BASP_CHECK_BOUNDS
+}
+
 template <int VEC>
 __global__ void __launch_bounds__(kThreads)
 basp_relayout_kernel(const __grid_constant__ Params p) {
-    using W = typename Word<VEC>::T;
 #if BASP_PDL
     // Launched with programmatic stream serialisation: the previous kernel on
-    // the stream may still be running.  Wait for it (and its memory) before
-    // touching any buffer, then let the next kernel start its own launch.
+    // the stream may still be running.  CTAs below p.prefetch_ctas (all of
+    // them by default) warm L2 with their first tile's source lines: in the
+    // CTAs resident that early the DRAM latency of the first loads overlaps
+    // the previous kernel's tail, and in every CTA the line requests go out
+    // ahead of the loads without holding registers.  Then every CTA waits for
+    // that kernel (and its memory) before touching any buffer, and lets the
+    // next kernel start its own launch.  The tile is located again after the
+    // wait, so nothing stays live across it.
+    if (blockIdx.x < p.prefetch_ctas && blockIdx.x < p.total_tiles)
+        prefetch_tile<VEC>(locate(p, blockIdx.x));
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" :::);
 #endif
-    for (uint32_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-        int jb = 0;
-        if (p.njobs > 1 && t >= p.job[1].tile_begin) jb = 1;
-        if (p.njobs > 2 && t >= p.job[2].tile_begin) jb = 2;
-        const Job &J = p.job[jb];
-
-        // tile -> (block digits, tile within block).  Tiles run either block
-        // by block (inner_fast = 0) or with the innermost block digit varying
-        // fastest, so that consecutive tiles fill neighbouring row segments.
-        uint32_t lt = t - J.tile_begin;
-        uint32_t tb, q;
-        int64_t sb = 0, db = 0;
-        if (J.inner_fast) {
-            q = lt / J.radix[3];
-            const uint32_t d3 = lt - q * J.radix[3];
-            sb += int64_t(d3) * J.src_bs[3];
-            db += int64_t(d3) * J.dst_bs[3];
-            lt = q;
-            q = lt / J.tiles_per_block;
-            tb = lt - q * J.tiles_per_block;
-            lt = q;
-        } else {
-            q = lt / J.tiles_per_block;
-            tb = lt - q * J.tiles_per_block;
-            lt = q;
-            q = lt / J.radix[3];
-            const uint32_t d3 = lt - q * J.radix[3];
-            sb += int64_t(d3) * J.src_bs[3];
-            db += int64_t(d3) * J.dst_bs[3];
-            lt = q;
-        }
-#pragma unroll
-        for (int k = 2; k >= 1; --k) {
-            q = lt / J.radix[k];
-            const uint32_t dgt = lt - q * J.radix[k];
-            sb += int64_t(dgt) * J.src_bs[k];
-            db += int64_t(dgt) * J.dst_bs[k];
-            lt = q;
-        }
-        sb += int64_t(lt) * J.src_bs[0];
-        db += int64_t(lt) * J.dst_bs[0];
-
-        const uint32_t i0 = tb * uint32_t(kTileVec);
-        const uint32_t i1 = min(i0 + uint32_t(kTileVec), J.vec_per_block);
-        const W *src = reinterpret_cast<const W *>(J.src) + sb;
-        W *dst = reinterpret_cast<W *>(J.dst) + db;
-
-#if BASP_CHECK_BOUNDS
-        (void)src;
-        (void)dst;
-        for (int u = 0; u < kUnroll; ++u) {
-            const uint32_t i = i0 + threadIdx.x + uint32_t(u * kThreads);
-            if (i < i1) {
-                const uint32_t row = (__umulhi(i, J.vpr_magic) + i) >> J.vpr_shift;
-                const uint32_t col = i - row * J.vpr;
-                const int64_t so = sb + int64_t(row) * J.src_rs + col;
-                const int64_t dof = db + int64_t(row) * J.dst_rs + col;
-                if (so < J.src_lo || so >= J.src_hi || dof < J.dst_lo || dof >= J.dst_hi) {
-                    atomicAdd(&g_basp_bounds_violations, 1ull);
-                    continue;
-                }
-                store(reinterpret_cast<W *>(J.dst) + dof,
-                      load_stream(reinterpret_cast<const W *>(J.src) + so));
-            }
-        }
-#else
-        W v[kUnroll];
-#if !BASP_RECOMPUTE_DST
-        int64_t doff[kUnroll];
-#endif
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const uint32_t i = i0 + threadIdx.x + uint32_t(u * kThreads);
-            if (i < i1) {
-                const uint32_t row = (__umulhi(i, J.vpr_magic) + i) >> J.vpr_shift;
-                const uint32_t col = i - row * J.vpr;
-                v[u] = load_stream(src + (int64_t(row) * J.src_rs + col));
-#if !BASP_RECOMPUTE_DST
-                doff[u] = int64_t(row) * J.dst_rs + col;
-#endif
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const uint32_t i = i0 + threadIdx.x + uint32_t(u * kThreads);
-            if (i < i1) {
-#if BASP_RECOMPUTE_DST
-                const uint32_t row = (__umulhi(i, J.vpr_magic) + i) >> J.vpr_shift;
-                const uint32_t col = i - row * J.vpr;
-                store(dst + (int64_t(row) * J.dst_rs + col), v[u]);
-#else
-                store(dst + doff[u], v[u]);
-#endif
-            }
-        }
-#endif  // BASP_CHECK_BOUNDS
-    }
+    for (uint32_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x)
+        copy_tile<VEC>(locate(p, t));
 }
 
 }  // namespace

@@ -49,5 +49,12 @@ def _family():
 
 WORKLOADS = {w.name: w for w in _family()}
 
-# The shape the headline bench line is quoted on.
-HEADLINE = "llama3.2-1b_B2_S8192"
+# The shape the headline bench line is quoted on: the largest one (Llama-3.2-3B
+# heads, B=2, S=32768), the end of the sequence-length sweep.
+HEADLINE = "llama3.2-3b_B2_S32768"
+
+# The long-sequence shapes at which the fused kernel should run at >= 80% of the
+# HBM copy bandwidth in both directions and both layouts; the bench line
+# carries a roofline for each.
+TARGETS = ("qwen1.5-1.8b_B2_S16384", "llama3.2-3b_B2_S16384", "llama3.2-3b_B2_S32768")
+TARGET_FRACTION = 0.8

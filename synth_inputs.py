@@ -66,6 +66,15 @@ def bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(BITS[t.dtype]).numpy()
 
 
+def normal_device(n: int, seed: int, dtype: str, device) -> torch.Tensor:
+    """Like :func:`normal`, drawn by the device's own generator (the bench's
+    full-size buffers; the values differ from the CPU draw of the same seed)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    x = torch.randn(int(n), generator=g, dtype=torch.float32, device=device)
+    return x.to(DTYPES[dtype])
+
+
 def random_bits_device(n: int, seed: int, dtype: str, device) -> torch.Tensor:
     """Like :func:`random_bits`, drawn by the device's own generator (for
     buffers too large to draw on the CPU in a test's time)."""

@@ -287,3 +287,27 @@ def test_binding_refuses_bad_tensors():
         packed = torch.empty(L.info["bytes_qkv_packed"] // 2 - 1, dtype=torch.bfloat16)
         with pytest.raises(ValueError, match="bytes"):
             basp.basp_seq2head_qkv(L.handle, packed, FAKE, FAKE + 2 * nq, FAKE + 4 * nq)
+
+
+def test_binding_refuses_a_tensor_on_another_device(monkeypatch):
+    """A CUDA tensor on a device other than the current one is refused before
+    the C call (the library launches on the current device).  A stand-in
+    tensor plays cuda:1 so this runs without a GPU."""
+    from sequence_re_layout_gb300 import binding
+
+    class OnDevice1:
+        is_cuda = True
+        nbytes = 1 << 30
+        device = type("Dev", (), {"index": 1})()
+
+        def is_contiguous(self):
+            return True
+
+        def data_ptr(self):
+            return FAKE
+
+    monkeypatch.setattr(binding, "_current_device", lambda: 0)
+    with basp.Layout(2, 64, 8, 4, 16, 4, 2, "bf16") as L:
+        with pytest.raises(ValueError, match="current device is cuda:0"):
+            basp.basp_seq2head(L.handle, "fused", OnDevice1(), None, None,
+                               FAKE + (1 << 31), None, None)

@@ -113,3 +113,49 @@ def test_peak_file_forms(tmp_path, monkeypatch, content, expect):
 def test_peak_file_absent(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.hbm_peak() == (bench.FALLBACK_HBM_GBS, "fallback")
+
+
+def _run_bench(args, env_extra=None, timeout=600):
+    env = dict(os.environ)
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "LOCAL_WORLD_SIZE", "MASTER_ADDR",
+              "MASTER_PORT"):
+        env.pop(k, None)
+    env.update(env_extra or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args,
+                          capture_output=True, text=True, timeout=timeout, cwd=ROOT,
+                          env=env)
+
+
+def test_gpus_flag_starts_that_many_ranks():
+    """--gpus 2 with no launcher environment starts two local ranks (each
+    with its own RANK / LOCAL_RANK), and rank 0's line reports both."""
+    r = _run_bench(["--impl", "reference", "--gpus", "2", "--steps", "1",
+                    "--warmup", "1", "--config", "tiny_B2_N4_S64_H4_d16_fp32"])
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout          # rank 0 alone prints
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2 and line["impl"] == "reference"
+
+
+def test_gpus_flag_must_agree_with_the_launcher():
+    """A launcher's WORLD_SIZE that disagrees with --gpus is an error, not a
+    silent run at the launcher's size."""
+    r = _run_bench(["--impl", "reference", "--gpus", "4", "--steps", "1",
+                    "--warmup", "1", "--config", "tiny_B2_N4_S64_H4_d16_fp32"],
+                   env_extra={"WORLD_SIZE": "1", "RANK": "0", "LOCAL_RANK": "0"})
+    assert r.returncode != 0
+    assert "must agree" in r.stderr
+
+
+def test_timing_check_flags_impossible_kernel_times():
+    """The cross-check of per-kernel launch times against the step time."""
+    peak = 6700.0
+    # 200 MB + 130 MB in 31 us + 20 us against a 51 us step: consistent
+    ok = bench.check_timings(200e6, 0.031, 130e6, 0.020, 0.051, peak)
+    assert ok["consistent"] and ok["plausible"]
+    # a slow seq2head reading (43 us) leaves 10 us for 130 MB of head2seq:
+    # 13 TB/s, above any copy peak
+    bad = bench.check_timings(200e6, 0.043, 130e6, 0.020, 0.053, peak)
+    assert not bad["plausible"] and not bad["consistent"]
+    assert bad["implied_head2seq_gbs"] > 1.15 * peak

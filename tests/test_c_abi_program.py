@@ -64,3 +64,16 @@ def test_cpp_layer_on_gpu(cpp_program):
     r = subprocess.run([cpp_program, "gpu"], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     assert "abi_example_cpp ok" in r.stdout
+
+
+def test_scratch_address_cache_follows_the_context(tmp_path):
+    """The no-allocation entry point caches its scratch array's device address
+    per CUDA context: a new context (as after a device reset) gets a fresh
+    lookup, never the old address.  Host test with a fake context query."""
+    exe = str(tmp_path / "scratch_cache_test")
+    subprocess.run(["g++", "-std=c++17", "-O1", "-pthread", "-o", exe,
+                    os.path.join(ROOT, "tests", "c", "scratch_cache_test.cpp"),
+                    "-I", os.path.join(ROOT, "sequence_re_layout_gb300", "csrc")], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    assert "scratch_cache ok" in r.stdout

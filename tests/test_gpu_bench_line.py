@@ -22,17 +22,30 @@ def _run(*args):
 
 
 def test_default_line_has_the_contract_fields():
-    d = _run("--steps", "20", "--warmup", "3", "--soak-s", "0.2", "--cpu-baseline-s", "1")
+    d = _run("--steps", "20", "--warmup", "3", "--soak-s", "0.2", "--cpu-baseline-s", "1",
+             "--cpu-all-s", "1")
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
                 "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
         assert key in d, key
     assert d["steps"] == 20 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["value"] > 1000 and d["unit"] == "GB/s" and d["higher_is_better"] is True
-    assert d["config"]["workload"] == "llama3.2-1b_B2_S8192"
+    assert d["config"]["workload"] == "llama3.2-3b_B2_S32768"
     r = d["roofline"]
     assert r["bound"] == "hbm" and 0 < r["frac"] < 1.5 and r["achieved"] > 0
-    assert set(("value", "unit", "cores", "kind", "sample")) <= set(d["cpu_baseline"])
+    # the per-kernel times add up to the step time
+    assert d["timing_check"]["consistent"] and d["timing_check"]["plausible"]
+    c = d["cpu_baseline"]
+    assert set(("value", "unit", "cores", "kind", "sample")) <= set(c)
+    assert c["threads_1"]["value"] > 0 and c["threads_all"]["threads"] == c["cores"] >= 1
+    # every long-sequence target, both layouts, both directions
+    t = d["targets"]
+    got = {(l["workload"], l["layout"]) for l in t["legs"]}
+    assert got == {(w, lay) for w in ("qwen1.5-1.8b_B2_S16384", "llama3.2-3b_B2_S16384",
+                                      "llama3.2-3b_B2_S32768")
+                   for lay in ("basp", "ulysses")}
+    for l in t["legs"]:
+        assert l["seq2head"]["frac"] > 0 and l["head2seq"]["frac"] > 0, l
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] > 0

@@ -4,14 +4,16 @@ library's built-in scratch, for callers that cannot allocate device memory
 a serving loop that bans cudaMalloc on its hot path).
 
 Two calls in a row through the C ABI, each on fresh inputs, must give the same
-bits as the ordinary entry point basp_seq2head (and hence the oracle); a call
+bits as the ordinary entry point basp_seq2head and as the CPU oracle; a call
 whose scratch would exceed the built-in buffer is refused before any launch.
 This file is collected last on purpose: it shares no state with the others
 and passes alone or after them.
 """
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth_inputs
 import sequence_re_layout_gb300 as basp
 
@@ -43,9 +45,13 @@ def test_noalloc_matches_seq2head_on_two_calls(shape, dtype, order):
             basp.basp_seq2head(L.handle, "fused", *ins, *want)
             basp.basp_seq2head_noalloc(L.handle, *ins, *got)
             torch.cuda.synchronize()
-            for name, g, w in zip("qkv", got, want):
+            for name, g, w, x, H in zip("qkv", got, want, ins, (Hq, Hkv, Hkv)):
                 assert torch.equal(g.view(bits), w.view(bits)), \
-                    "call %d tensor %s differs" % (call, name)
+                    "call %d tensor %s differs from basp_seq2head" % (call, name)
+                exp = oracle.seq2head(synth_inputs.bits(x.cpu()), B, S, H, d, N, K,
+                                      order=order)
+                assert np.array_equal(synth_inputs.bits(g.cpu()), exp), \
+                    "call %d tensor %s differs from the oracle" % (call, name)
 
 
 def test_noalloc_refuses_more_than_its_scratch():
