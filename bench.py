@@ -291,6 +291,29 @@ def gbs(nbytes, ms):
     return nbytes / (ms * 1e-3) / 1e9
 
 
+def copy_rate_same_run(dev, n_elems=1 << 30, reps=10):
+    """torch's copy_ of n_elems bf16 elements (read + write bytes), best of
+    `reps`, CUDA events: the same kind of figure as the measured peak, taken
+    in this run on this GPU, as a cross-check of the fractions."""
+    import torch
+    a = torch.empty(n_elems, dtype=torch.bfloat16, device=dev)
+    b = torch.empty_like(a)
+    a.fill_(1.0)
+    b.copy_(a)
+    best = math.inf
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        b.copy_(a)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        best = min(best, e0.elapsed_time(e1))
+    del a, b
+    torch.cuda.empty_cache()
+    return gbs(2 * 2 * n_elems, best)
+
+
 def check_timings(s2h_bytes, s2h_ms, h2s_bytes, h2s_ms, step_ms, peak):
     """Cross-check the per-kernel launch times against the step time measured
     separately: the two kernels' times should add up to the step's (within
@@ -464,6 +487,23 @@ def run_device(w, layout, algo, steps, warmup, dev, peak, soak_s=0.0, order="bsh
     chk, steady_ms, n_steady, s2h_ms, n_s2h, h2s_ms, n_h2s = attempts[-1]
     chk["attempts"] = len(attempts)
 
+    # distribution: 30 windows of whole steps back to back, events only
+    # between windows (so programmatic launch overlaps every boundary but 29);
+    # each window lasts >= 2 ms
+    n_win = 30
+    per_win = max(5, int(math.ceil(2.0 / max(est_step, 1e-4))))
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_win + 1)]
+    timed(step, 20)
+    evs[0].record(stream)
+    i = 0
+    for k in range(n_win):
+        for _ in range(per_win):
+            step(i)
+            i += 1
+        evs[k + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    win_ms = [evs[k].elapsed_time(evs[k + 1]) / per_win for k in range(n_win)]
+
     # spread: the same K-step loop repeated (only reported, never the value)
     repeats = [timed(step, steps) / steps for _ in range(spread)]
     launches_per_step = 2 * passes
@@ -480,12 +520,34 @@ def run_device(w, layout, algo, steps, warmup, dev, peak, soak_s=0.0, order="bsh
         "timed_launches": launches_per_step * steps,
         "total_launches": count[0],
         "repeat_ms_per_step": repeats,
+        "window_ms_per_step": win_ms, "steps_per_window": per_win,
         "wall": (soak_t0 if soak_s > 0 else t0, t1),
     }
     del sets, ws
     L.close()
     torch.cuda.empty_cache()
     return res
+
+
+def percentile(xs, q):
+    """The q-th percentile (0..100) of xs, linear between closest ranks."""
+    xs = sorted(xs)
+    if not xs:
+        return None
+    pos = (len(xs) - 1) * q / 100.0
+    lo = int(math.floor(pos))
+    hi = min(lo + 1, len(xs) - 1)
+    return xs[lo] + (xs[hi] - xs[lo]) * (pos - lo)
+
+
+def window_stats(r):
+    """GB/s over the run's 30 step windows: median, p10 and p90."""
+    g = [gbs(r["step_bytes"], ms) for ms in r["window_ms_per_step"]]
+    return {"windows": len(g), "steps_per_window": r["steps_per_window"],
+            "gbs_p10": round(percentile(g, 10), 2), "gbs_median": round(percentile(g, 50), 2),
+            "gbs_p90": round(percentile(g, 90), 2),
+            "note": "events only between windows; each window's first launch waits for the "
+                    "last one's completion, so windows read a little below the back-to-back loop"}
 
 
 def kernel_roofline(nbytes, ms, peak, traffic, plausible):
@@ -516,6 +578,7 @@ def leg_summary(w, layout, r, peak, order="bshd", packed=False, algo="fused"):
             "steady_step": {"gbs": round(steady, 2), "frac": round(steady / peak, 4),
                             "ms": round(r["steady_ms_per_step"], 6),
                             "steps": r["steady_steps"]},
+            "distribution": window_stats(r),
             "check": r["check"]}
 
 
@@ -714,6 +777,7 @@ def main_ours(args, dist):
                             "timed region; `value` is the timed region alone"
                             % args.window_ms),
         "timing_check": head["check"],
+        "distribution": head["distribution"],
         "analytic": {"peers_per_rank": info["peers"],
                      "bytes_per_peer_q": info["bytes_per_peer_q"],
                      "bytes_per_peer_kv": info["bytes_per_peer_kv"],
@@ -820,6 +884,12 @@ def main_ours(args, dist):
                               "peak_kind": "of %s" % peak_kind,
                               "all_meet_bar": all(l["meets_bar"] for l in tl),
                               "legs": tl}
+        cr = copy_rate_same_run(dev)
+        out["roofline"]["copy_same_run"] = {
+            "gbs": round(cr, 2), "kernel_vs_copy": round(s2h["achieved"] / cr, 4)
+            if s2h["achieved"] else None,
+            "how": "torch copy_ of 1 Gi bf16 elements, read + write bytes, best of 10, "
+                   "in this run (the kind of copy MEASURED_PEAKS.json records)"}
         if dist.world == 1:
             out["cpu_baseline"] = cpu_baseline(w, args.layout, args.cpu_baseline_s,
                                                args.cpu_all_s, order=args.order)

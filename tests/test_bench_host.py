@@ -159,3 +159,14 @@ def test_timing_check_flags_impossible_kernel_times():
     bad = bench.check_timings(200e6, 0.043, 130e6, 0.020, 0.053, peak)
     assert not bad["plausible"] and not bad["consistent"]
     assert bad["implied_head2seq_gbs"] > 1.15 * peak
+
+
+def test_percentiles():
+    xs = [float(x) for x in range(1, 11)]          # 1..10
+    assert bench.percentile(xs, 50) == 5.5
+    assert bench.percentile(xs, 10) == 1.9
+    assert bench.percentile(xs, 90) == 9.1
+    assert bench.percentile([3.0], 90) == 3.0
+    r = {"step_bytes": 1e9, "window_ms_per_step": [1.0, 2.0, 0.5], "steps_per_window": 7}
+    st = bench.window_stats(r)
+    assert st["gbs_median"] == 1000.0 and st["windows"] == 3 and st["steps_per_window"] == 7

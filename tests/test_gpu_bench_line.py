@@ -33,6 +33,11 @@ def test_default_line_has_the_contract_fields():
     assert d["config"]["workload"] == "llama3.2-3b_B2_S32768"
     r = d["roofline"]
     assert r["bound"] == "hbm" and 0 < r["frac"] < 1.5 and r["achieved"] > 0
+    # a distribution over 30 step windows
+    dd = d["distribution"]
+    assert dd["windows"] == 30 and dd["gbs_p10"] <= dd["gbs_median"] <= dd["gbs_p90"]
+    # the same-run copy rate sits beside the measured peak
+    assert r["copy_same_run"]["gbs"] > 1000
     # the per-kernel times add up to the step time
     assert d["timing_check"]["consistent"] and d["timing_check"]["plausible"]
     c = d["cpu_baseline"]
