@@ -46,11 +46,15 @@
  *     handle may run concurrently from several host threads.
  *   - Kernels are launched with programmatic dependent launch: they may be
  *     scheduled while the previous kernel on `stream` drains, but wait for it
- *     (and its memory) before touching any buffer, so ordering on `stream` is
- *     as usual.  They also release the next kernel early; a kernel the caller
- *     launches after them with the programmatic-serialisation attribute must
- *     wait (cudaGridDependencySynchronize) before reading their outputs, as
- *     CUDA requires of every such kernel.
+ *     (and its memory) before reading or writing any buffer, so ordering on
+ *     `stream` is as usual.  Before that wait they ask L2 to fetch the lines
+ *     of their input (prefetch.global.L2): this reads no value into the
+ *     kernel, so an input the previous kernel is still writing is read only
+ *     after it has finished, with its final contents.  They also release the
+ *     next kernel early; a kernel the caller launches after them with the
+ *     programmatic-serialisation attribute must wait
+ *     (cudaGridDependencySynchronize) before reading their outputs, as CUDA
+ *     requires of every such kernel.
  */
 #ifndef BASP_H
 #define BASP_H
