@@ -63,3 +63,36 @@ def test_sequence_first_packed_line():
              "--order", "sbhd", "--qkv-packed", "--config", "llama3.2-3b_B2_S4096")
     assert d["config"]["order"] == "sbhd" and d["config"]["qkv_packed"] is True
     assert d["value"] > 1000
+
+
+def _two_rank_check(d):
+    assert d["n_gpus"] == 2 and d["config"]["parallelism"] == "replicas"
+    assert d["scaling"] == "weak" and d["value"] > 1000
+    # value is both ranks' bytes over the slower rank's time
+    assert abs(d["value"] - 2 * d["config"]["bytes_per_step"] / (d["ms_per_step"] * 1e6)) \
+        < 0.01 * d["value"]
+
+
+def test_two_replicas_started_by_the_gpus_flag():
+    """--gpus 2 with no launcher: two local ranks (here both on cuda:0; their
+    kernels never wait on each other, the ranks meet only at host barriers)."""
+    _two_rank_check(_run("--gpus", "2", "--steps", "5", "--warmup", "2", "--soak-s", "0",
+                         "--no-extras", "--config", "llama3.2-3b_B2_S4096"))
+
+
+def test_two_replicas_under_torchrun():
+    """The driver's multi-GPU launch: torchrun with --nproc-per-node 2."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                        "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                        "--gpus", "2", "--steps", "5", "--warmup", "2", "--soak-s", "0",
+                        "--no-extras", "--config", "llama3.2-3b_B2_S4096"],
+                       capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    _two_rank_check(json.loads(lines[0]))
