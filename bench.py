@@ -42,7 +42,10 @@ METRIC = ("seq↔head re-layout GB/s (read+write) and % of GB300 HBM peak, "
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
-KERNEL_SOURCE = os.path.join(ROOT, "sequence_re_layout_gb300", "csrc", "relayout_kernel.cuh")
+# the sources a traffic capture depends on: the kernel and the launch planning
+# (tile order, grid, prefetch) in relayout.cu
+KERNEL_SOURCES = tuple(os.path.join(ROOT, "sequence_re_layout_gb300", "csrc", f)
+                       for f in ("relayout_kernel.cuh", "relayout.cu"))
 # A kernel (or the rest of a step) reported above this multiple of the
 # measured copy bandwidth is not believed: the copy peak is itself a
 # read+write of the same bytes, so a permutation can match it, not exceed it
@@ -253,17 +256,18 @@ class ClockSampler:
 
 
 def source_digest():
-    """Digest of the kernel source's code: comments and blank space removed,
-    so a comment edit does not orphan a traffic record."""
+    """Digest of the code of the kernel and its launch planning: comments and
+    blank space removed, so a comment edit does not orphan a traffic record."""
     import re
-    with open(KERNEL_SOURCE) as f:
-        text = f.read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     code = []
-    for line in text.splitlines():
-        line = line.split("//", 1)[0].strip()
-        if line:
-            code.append(" ".join(line.split()))
+    for path in KERNEL_SOURCES:
+        with open(path) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for line in text.splitlines():
+            line = line.split("//", 1)[0].strip()
+            if line:
+                code.append(" ".join(line.split()))
     return hashlib.sha256("\n".join(code).encode()).hexdigest()[:16]
 
 
