@@ -105,28 +105,47 @@ def launch_local_ranks(n: int, argv) -> int:
     WORLD_SIZE in each one's environment, rendezvous on 127.0.0.1), as
     torchrun would.  Returns the first non-zero exit code, else 0; when one
     rank fails, the others are stopped."""
+    import signal
     port = _free_port()
     procs = []
-    for r in range(n):
-        env = dict(os.environ, WORLD_SIZE=str(n), RANK=str(r), LOCAL_RANK=str(r),
-                   LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1",
-                   MASTER_PORT=str(port))
-        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__)] + list(argv),
-                                      env=env))
-    rc = 0
-    live = list(procs)
-    while live:
-        for p in list(live):
-            code = p.poll()
-            if code is None:
-                continue
-            live.remove(p)
-            if code != 0 and rc == 0:
-                rc = code
-                for q in live:
-                    q.terminate()
-        time.sleep(0.05)
-    return rc
+
+    def stop_all(signum, frame):
+        # a signal to this process (a timeout, ^C) ends the ranks too
+        for q in procs:
+            if q.poll() is None:
+                q.terminate()
+        for q in procs:
+            try:
+                q.wait(timeout=10)
+            except subprocess.TimeoutExpired:
+                q.kill()
+        sys.exit(128 + signum)
+
+    old = {sig: signal.signal(sig, stop_all) for sig in (signal.SIGTERM, signal.SIGINT)}
+    try:
+        for r in range(n):
+            env = dict(os.environ, WORLD_SIZE=str(n), RANK=str(r), LOCAL_RANK=str(r),
+                       LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1",
+                       MASTER_PORT=str(port))
+            procs.append(subprocess.Popen(
+                [sys.executable, os.path.abspath(__file__)] + list(argv), env=env))
+        rc = 0
+        live = list(procs)
+        while live:
+            for p in list(live):
+                code = p.poll()
+                if code is None:
+                    continue
+                live.remove(p)
+                if code != 0 and rc == 0:
+                    rc = code
+                    for q in live:
+                        q.terminate()
+            time.sleep(0.05)
+        return rc
+    finally:
+        for sig, h in old.items():
+            signal.signal(sig, h)
 
 
 class Dist:

@@ -170,3 +170,29 @@ def test_percentiles():
     r = {"step_bytes": 1e9, "window_ms_per_step": [1.0, 2.0, 0.5], "steps_per_window": 7}
     st = bench.window_stats(r)
     assert st["gbs_median"] == 1000.0 and st["windows"] == 3 and st["steps_per_window"] == 7
+
+
+def test_launcher_stops_its_ranks_on_sigterm(tmp_path):
+    """A SIGTERM to the --gpus launcher ends the ranks it started (no orphans
+    left holding GPUs after a timeout)."""
+    import signal
+    import time as _t
+    env = dict(os.environ)
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    # a reference run long enough to be interrupted (many steps of a big shape)
+    p = subprocess.Popen([sys.executable, os.path.join(ROOT, "bench.py"), "--impl",
+                          "reference", "--gpus", "2", "--steps", "100000", "--warmup", "0",
+                          "--config", "llama3.2-1b_B2_S8192"],
+                         cwd=ROOT, env=env, stdout=subprocess.DEVNULL,
+                         stderr=subprocess.DEVNULL, start_new_session=True)
+    _t.sleep(8)
+    # rank 1 of the reference arm exits at once; rank 0 is still working
+    kids = subprocess.run(["pgrep", "-P", str(p.pid)], capture_output=True, text=True).stdout.split()
+    assert kids, "no rank running"
+    p.send_signal(signal.SIGTERM)
+    p.wait(timeout=60)
+    _t.sleep(1)
+    for k in kids:
+        assert not os.path.exists("/proc/%s" % k) or \
+            open("/proc/%s/stat" % k).read().split()[2] == "Z", "rank %s still running" % k
