@@ -41,7 +41,7 @@ METRIC = ("seq↔head re-layout GB/s (read+write) and % of GB300 HBM peak, "
           "BASP vs Ulysses")
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "basp_relayout_kernel_all_workloads_dram_traffic.txt")
 # the sources a traffic capture depends on: the kernel and the launch planning
 # (tile order, grid, prefetch) in relayout.cu
 KERNEL_SOURCES = tuple(os.path.join(ROOT, "sequence_re_layout_gb300", "csrc", f)
