@@ -196,3 +196,15 @@ def test_launcher_stops_its_ranks_on_sigterm(tmp_path):
     for k in kids:
         assert not os.path.exists("/proc/%s" % k) or \
             open("/proc/%s/stat" % k).read().split()[2] == "Z", "rank %s still running" % k
+
+
+def test_committed_traffic_matches_the_current_kernel():
+    """The ncu traffic record under profiles/ was taken on the kernel and
+    launch planning that are in the tree now, for the headline and every
+    target leg (else the bench would report traffic = null: recapture after
+    changing relayout_kernel.cuh or relayout.cu)."""
+    from sequence_re_layout_gb300.workloads import HEADLINE, TARGETS
+    for wl in (HEADLINE,) + tuple(TARGETS):
+        for lay in ("basp", "ulysses"):
+            for role in ("seq2head_qkv_fused", "head2seq_o_fused"):
+                assert bench.ncu_traffic(wl, lay, role) is not None, (wl, lay, role)
