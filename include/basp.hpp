@@ -79,6 +79,24 @@ public:
                       cudaStream_t stream) const {
         check(basp_head2seq_qkv(handle_, q, k, v, qkv_out, stream), "basp_head2seq_qkv");
     }
+    // host buffers in and out: staged through caller-owned device `staging`,
+    // or (staging null) read and written in place when page-locked
+    void seq2head_host(const void *q, const void *k, const void *v, void *q_out,
+                       void *k_out, void *v_out, void *staging, size_t staging_bytes,
+                       cudaStream_t stream, basp_algo algo = BASP_ALGO_FUSED,
+                       void *workspace = nullptr, size_t workspace_bytes = 0) const {
+        check(basp_seq2head_host(handle_, algo, q, k, v, q_out, k_out, v_out, staging,
+                                 staging_bytes, workspace, workspace_bytes, stream),
+              "basp_seq2head_host");
+    }
+    void head2seq_host(const void *o, const void *k, const void *v, void *o_out,
+                       void *k_out, void *v_out, void *staging, size_t staging_bytes,
+                       cudaStream_t stream, basp_algo algo = BASP_ALGO_FUSED,
+                       void *workspace = nullptr, size_t workspace_bytes = 0) const {
+        check(basp_head2seq_host(handle_, algo, o, k, v, o_out, k_out, v_out, staging,
+                                 staging_bytes, workspace, workspace_bytes, stream),
+              "basp_head2seq_host");
+    }
 
 private:
     basp_layout *handle_ = nullptr;

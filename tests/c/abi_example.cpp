@@ -57,6 +57,27 @@ static void gpu_checks() {
     CHECK(std::memcmp(out.data(), ref.data(), n * 2) == 0, "seq2head differs from the oracle");
     CHECK(std::memcmp(back.data(), h.data(), n * 2) == 0, "round trip differs");
     cudaFree(din); cudaFree(dout); cudaFree(dback);
+
+    // host buffers through the C++ layer: page-locked, re-laid out in place
+    // (no staging), then back; a pageable output is refused as an exception
+    void *pin_in, *pin_out, *pin_back;
+    CHECK(cudaMallocHost(&pin_in, n * 2) == cudaSuccess &&
+          cudaMallocHost(&pin_out, n * 2) == cudaSuccess &&
+          cudaMallocHost(&pin_back, n * 2) == cudaSuccess, "cudaMallocHost");
+    std::memcpy(pin_in, h.data(), n * 2);
+    L.seq2head_host(pin_in, nullptr, nullptr, pin_out, nullptr, nullptr, nullptr, 0, 0);
+    L.head2seq_host(pin_out, nullptr, nullptr, pin_back, nullptr, nullptr, nullptr, 0, 0);
+    CHECK(cudaDeviceSynchronize() == cudaSuccess, "sync");
+    CHECK(std::memcmp(pin_out, ref.data(), n * 2) == 0, "host seq2head differs from the oracle");
+    CHECK(std::memcmp(pin_back, h.data(), n * 2) == 0, "host round trip differs");
+    bool threw = false;
+    try {
+        L.seq2head_host(pin_in, nullptr, nullptr, out.data(), nullptr, nullptr, nullptr, 0, 0);
+    } catch (const basp::Error &e) {
+        threw = e.status() == BASP_ERR_WORKSPACE;
+    }
+    CHECK(threw, "pageable host output in direct mode must be refused");
+    cudaFreeHost(pin_in); cudaFreeHost(pin_out); cudaFreeHost(pin_back);
 }
 
 int main(int argc, char **argv) {

@@ -78,3 +78,31 @@ def test_producer_kernel_then_relayout_each_step():
             src[step::7] = -float(step)
             want = oracle.seq2head(synth_inputs.bits(src), B, S, Hq, d, N, K)
             assert np.array_equal(synth_inputs.bits(out.cpu()), want), step
+
+
+def test_qkv_projection_then_packed_seq2head():
+    """The path as a model runs it: a GEMM (the fused QKV projection) writes
+    the packed QKV activations, and basp_seq2head_qkv reads them right after,
+    on the same stream, step after step with new weights."""
+    B, S, Hq, Hkv, d, N, K = 2, 1024, 24, 8, 128, 8, 4
+    hidden = 256
+    W = (Hq + 2 * Hkv) * d
+    g = torch.Generator(device=DEV)
+    g.manual_seed(7)
+    x = torch.randn(N, B * S // N, hidden, generator=g, device=DEV).to(torch.bfloat16)
+    with basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16") as L:
+        nq, nkv = B * S * Hq * d, B * S * Hkv * d
+        qkv = torch.empty(N, B * S // N, W, dtype=torch.bfloat16, device=DEV)
+        outs = []
+        for step in range(4):
+            w = torch.randn(hidden, W, generator=g, device=DEV).to(torch.bfloat16)
+            torch.matmul(x, w, out=qkv)                       # the producer GEMM
+            o = [torch.empty(n, dtype=torch.bfloat16, device=DEV) for n in (nq, nkv, nkv)]
+            basp.basp_seq2head_qkv(L.handle, qkv, *o)
+            outs.append((qkv.clone(), o))                     # snapshot after the call
+        torch.cuda.synchronize()
+        for step, (packed, o) in enumerate(outs):
+            want = oracle.seq2head_qkv(synth_inputs.bits(packed.view(-1).cpu()),
+                                       B, S, Hq, Hkv, d, N, K)
+            for name, got, e in zip("qkv", o, want):
+                assert np.array_equal(synth_inputs.bits(got.cpu()), e), (step, name)
