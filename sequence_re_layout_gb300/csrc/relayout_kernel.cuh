@@ -6,8 +6,9 @@
 // vectors).  A tile lies inside one block of rows (fixed g, j, jp, bl); the
 // block's source and destination bases come from its four digits times the
 // job's stride tables, and vector i of the block sits in row i / vpr,
-// column i % vpr.  Loads are non-coherent and skip L1; stores are
-// evict-first.  Every thread issues its kUnroll loads before its stores.
+// column i % vpr.  Loads are non-coherent and skip L1; stores are plain
+// (the written lines stay in L2 at normal priority).  Every thread issues
+// its kUnroll loads before its stores.
 // Every CTA first prefetches its tile's source lines into L2; the ones
 // resident before the previous kernel on the stream has finished do so while
 // it drains, before they wait for it.
@@ -40,7 +41,7 @@ namespace {
 #define BASP_UNROLL 4
 #endif
 #ifndef BASP_STORE_CS
-#define BASP_STORE_CS 1
+#define BASP_STORE_CS 0         // plain stores: with the L2 prefetch they beat .cs
 #endif
 #ifndef BASP_RECOMPUTE_DST
 #define BASP_RECOMPUTE_DST 0
