@@ -788,7 +788,7 @@ def main_ours(args, dist):
         "pct_hbm_peak": round(100 * value / dist.world / peak, 2),
         "pct_hbm_nominal": round(100 * value / dist.world / NOMINAL_HBM_GBS, 2),
         "roofline": dict({
-            "bound": "hbm", "kernel": "basp_relayout_kernel<16> (seq2head Q,K,V)",
+            "bound": "hbm", "kernel": "basp_relayout_kernel (seq2head Q,K,V)",
             "peak": peak, "unit": "GB/s",
             "launch_timing": "CUDA events around %d back-to-back launches of this "
                              "kernel alone on the bench stream, after 20 untimed "

@@ -195,7 +195,7 @@ int pick_vec(const basp_layout &L, const TensorArg *t, int n,
 }
 
 basp_status plan(const basp_layout &L, const Pass &pass, const TensorArg *t,
-                 int n, int vec, Params *p) {
+                 int n, int vec, int tile_vec, Params *p) {
     std::memset(p, 0, sizeof(*p));
     uint64_t tiles = 0;
     int nj = 0;
@@ -234,7 +234,7 @@ basp_status plan(const basp_layout &L, const Pass &pass, const TensorArg *t,
         J.vpr = uint32_t(vpr);
         udiv_magic(J.vpr, &J.vpr_magic, &J.vpr_shift);
         J.vec_per_block = uint32_t(vec_per_block);
-        J.tiles_per_block = uint32_t((vec_per_block + kTileVec - 1) / kTileVec);
+        J.tiles_per_block = uint32_t((vec_per_block + tile_vec - 1) / tile_vec);
         J.tile_begin = uint32_t(tiles);
         J.inner_fast = uint32_t(pass.inner_fast);
         const uint64_t blocks = uint64_t(L.G) * L.K * L.K * uint64_t(extent_of(L, C_BL));
@@ -255,7 +255,7 @@ constexpr int kHostCtasPerSm = 1;
 // CTA slots of one wave on the current device: SMs x resident CTAs of the
 // kernel (persistent: at most kHostCtasPerSm per SM).  Cached per device (a
 // benign race: every thread computes the same value).
-template <int VEC>
+template <int VEC, int THREADS>
 uint32_t wave_slots(bool persistent) {
     static std::atomic<int> cache[2][64];
     int dev = 0;
@@ -265,7 +265,7 @@ uint32_t wave_slots(bool persistent) {
         int sms = 0, per_sm = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &per_sm, basp_relayout_kernel<VEC>, kThreads, 0) != cudaSuccess) {
+                &per_sm, basp_relayout_kernel<VEC, THREADS>, THREADS, 0) != cudaSuccess) {
             cudaGetLastError();           // clear the error this probe caused
             return 1;
         }
@@ -282,9 +282,9 @@ uint32_t wave_slots(bool persistent) {
 // kHostCtasPerSm CTAs per SM striding over the tiles.  The CTAs of a
 // device-memory grid prefetch their tile into L2 first (BASP_PREFETCH: all of
 // them, or those of the first wave); host memory is never prefetched.
-template <int VEC>
+template <int VEC, int THREADS = kThreads>
 basp_status launch_vec(Params p, cudaStream_t stream, bool persistent) {
-    const uint32_t slots = wave_slots<VEC>(persistent);
+    const uint32_t slots = wave_slots<VEC, THREADS>(persistent);
     uint32_t grid = p.total_tiles < slots ? p.total_tiles : slots;
     if (BASP_GRID_ALL_TILES && !persistent) grid = p.total_tiles;
     p.prefetch_ctas = 0;
@@ -293,7 +293,7 @@ basp_status launch_vec(Params p, cudaStream_t stream, bool persistent) {
 #if BASP_PDL
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -302,14 +302,14 @@ basp_status launch_vec(Params p, cudaStream_t stream, bool persistent) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // the launch's own status: an error the caller left pending is not ours
-    if (cudaLaunchKernelEx(&cfg, basp_relayout_kernel<VEC>, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, basp_relayout_kernel<VEC, THREADS>, p) != cudaSuccess) {
         cudaGetLastError();               // clear the error this launch set
         return BASP_ERR_CUDA;
     }
     return BASP_OK;
 #else
     cudaGetLastError();                   // start from a clean error state
-    basp_relayout_kernel<VEC><<<grid, kThreads, 0, stream>>>(p);
+    basp_relayout_kernel<VEC, THREADS><<<grid, THREADS, 0, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? BASP_OK : BASP_ERR_CUDA;
 #endif
 }
@@ -318,8 +318,23 @@ basp_status run_pass(const basp_layout &L, const Pass &pass,
                      const TensorArg *t, int n, int vec, cudaStream_t stream,
                      bool persistent = false) {
     Params p;
-    basp_status st = plan(L, pass, t, n, vec, &p);
+    basp_status st = plan(L, pass, t, n, vec, kThreads * kUnroll, &p);
     if (st != BASP_OK || p.total_tiles == 0) return st;
+    // A long launch (at least BASP_LARGE_WAVES waves of kThreads-thread CTAs)
+    // runs kThreadsLarge-thread CTAs with tiles as many vectors longer:
+    // measured on GB300, +0.4-0.5% from S=8192 up, while short launches
+    // lose with them (2.6% at S=1024).  Host memory keeps the persistent
+    // kThreads grid.
+    if constexpr (kThreadsLarge != kThreads) {
+        if (vec == 16 && !persistent &&
+            uint64_t(p.total_tiles) >=
+                uint64_t(BASP_LARGE_WAVES) * wave_slots<16, kThreads>(false)) {
+            Params q;
+            st = plan(L, pass, t, n, vec, kThreadsLarge * kUnroll, &q);
+            if (st != BASP_OK) return st;
+            return launch_vec<16, kThreadsLarge>(q, stream, false);
+        }
+    }
     switch (vec) {
         case 16: return launch_vec<16>(p, stream, persistent);
         case 8: return launch_vec<8>(p, stream, persistent);

@@ -2,8 +2,8 @@
 // every pass launches, its job table and its load/store helpers.  Included
 // once, by relayout.cu.
 //
-// Each CTA copies one tile of kThreads * kUnroll vectors (16 KiB at 16-byte
-// vectors).  A tile lies inside one block of rows (fixed g, j, jp, bl); the
+// Each CTA copies one tile of THREADS * kUnroll vectors (16 KiB at 16-byte
+// vectors and 256 threads; 32 KiB with the 512-thread CTAs of long launches).  A tile lies inside one block of rows (fixed g, j, jp, bl); the
 // block's source and destination bases come from its four digits times the
 // job's stride tables, and vector i of the block sits in row i / vpr,
 // column i % vpr.  Loads are non-coherent and skip L1; stores are plain
@@ -23,6 +23,8 @@ namespace {
 // Build-time tuning switches (-DBASP_...=); the defaults are the settings
 // that measured best on GB300.  None of them changes what is copied where.
 //   BASP_THREADS, BASP_UNROLL  tile shape: threads per CTA, vectors per thread
+//   BASP_THREADS_LARGE         threads per CTA of long launches (0: always
+//                              BASP_THREADS); BASP_LARGE_WAVES sets "long"
 //   BASP_STORE_CS              evict-first stores (1) or plain stores (0)
 //   BASP_RECOMPUTE_DST         recompute store offsets instead of keeping them
 //   BASP_CTAS_PER_SM           cap on resident CTAs for persistent grids
@@ -39,6 +41,12 @@ namespace {
 #endif
 #ifndef BASP_UNROLL
 #define BASP_UNROLL 4
+#endif
+#ifndef BASP_THREADS_LARGE
+#define BASP_THREADS_LARGE 512
+#endif
+#ifndef BASP_LARGE_WAVES
+#define BASP_LARGE_WAVES 8
 #endif
 #ifndef BASP_STORE_CS
 #define BASP_STORE_CS 0         // plain stores: with the L2 prefetch they beat .cs
@@ -62,8 +70,10 @@ namespace {
 #define BASP_PREFETCH 2
 #endif
 constexpr int kThreads = BASP_THREADS;   // threads per CTA
+// threads per CTA of launches of at least BASP_LARGE_WAVES waves of
+// kThreads-thread CTAs (device memory, 16-byte vectors)
+constexpr int kThreadsLarge = BASP_THREADS_LARGE > 0 ? BASP_THREADS_LARGE : BASP_THREADS;
 constexpr int kUnroll = BASP_UNROLL;     // vectors in flight per thread
-constexpr int kTileVec = kThreads * kUnroll;
 constexpr int kMaxJobs = 3;
 
 enum Coord { C_G = 0, C_J = 1, C_JP = 2, C_BL = 3, C_SL = 4 };
@@ -168,7 +178,9 @@ struct Tile {
 // tile -> (job, block digits, tile within block).  Tiles run either block by
 // block (inner_fast = 0) or with the innermost block digit varying fastest,
 // so that consecutive tiles fill neighbouring row segments.
+template <int THREADS>
 __device__ __forceinline__ Tile locate(const Params &p, uint32_t t) {
+    constexpr uint32_t kTile = uint32_t(THREADS * kUnroll);
     int jb = 0;
     if (p.njobs > 1 && t >= p.job[1].tile_begin) jb = 1;
     if (p.njobs > 2 && t >= p.job[2].tile_begin) jb = 2;
@@ -209,8 +221,8 @@ __device__ __forceinline__ Tile locate(const Params &p, uint32_t t) {
     T.J = &J;
     T.sb = sb;
     T.db = db;
-    T.i0 = tb * uint32_t(kTileVec);
-    T.i1 = min(T.i0 + uint32_t(kTileVec), J.vec_per_block);
+    T.i0 = tb * kTile;
+    T.i1 = min(T.i0 + kTile, J.vec_per_block);
     return T;
 }
 
@@ -224,14 +236,14 @@ __device__ __forceinline__ uint32_t row_of(const Job &J, uint32_t i) {
 // thread, so it may run before the previous kernel on the stream has finished:
 // L2 is where every SM's accesses meet, so a line that kernel writes later is
 // updated there, and the loads after griddepcontrol.wait see its final value.
-template <int VEC>
+template <int VEC, int THREADS>
 __device__ __forceinline__ void prefetch_tile(const Tile &T) {
     using W = typename Word<VEC>::T;
     const Job &J = *T.J;
     const W *src = reinterpret_cast<const W *>(J.src) + T.sb;
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-        const uint32_t i = T.i0 + threadIdx.x + uint32_t(u * kThreads);
+        const uint32_t i = T.i0 + threadIdx.x + uint32_t(u * THREADS);
         if (i < T.i1) {
             const uint32_t row = row_of(J, i);
             const int64_t so = int64_t(row) * J.src_rs + (i - row * J.vpr);
@@ -243,7 +255,7 @@ __device__ __forceinline__ void prefetch_tile(const Tile &T) {
     }
 }
 
-template <int VEC>
+template <int VEC, int THREADS>
 __device__ __forceinline__ void copy_tile(const Tile &T) {
     using W = typename Word<VEC>::T;
     const Job &J = *T.J;
@@ -251,7 +263,7 @@ __device__ __forceinline__ void copy_tile(const Tile &T) {
     W *dst = reinterpret_cast<W *>(J.dst) + T.db;
 #if BASP_CHECK_BOUNDS
     for (int u = 0; u < kUnroll; ++u) {
-        const uint32_t i = T.i0 + threadIdx.x + uint32_t(u * kThreads);
+        const uint32_t i = T.i0 + threadIdx.x + uint32_t(u * THREADS);
         if (i < T.i1) {
             const uint32_t row = row_of(J, i);
             const uint32_t col = i - row * J.vpr;
@@ -274,7 +286,7 @@ __device__ __forceinline__ void copy_tile(const Tile &T) {
 #endif
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-        const uint32_t i = T.i0 + threadIdx.x + uint32_t(u * kThreads);
+        const uint32_t i = T.i0 + threadIdx.x + uint32_t(u * THREADS);
         if (i < T.i1) {
             const uint32_t row = row_of(J, i);
             const uint32_t col = i - row * J.vpr;
@@ -286,7 +298,7 @@ __device__ __forceinline__ void copy_tile(const Tile &T) {
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-        const uint32_t i = T.i0 + threadIdx.x + uint32_t(u * kThreads);
+        const uint32_t i = T.i0 + threadIdx.x + uint32_t(u * THREADS);
         if (i < T.i1) {
 #if BASP_RECOMPUTE_DST
             const uint32_t row = row_of(J, i);
@@ -299,8 +311,8 @@ __device__ __forceinline__ void copy_tile(const Tile &T) {
 #endif  // BASP_CHECK_BOUNDS
 }
 
-template <int VEC>
-__global__ void __launch_bounds__(kThreads)
+template <int VEC, int THREADS>
+__global__ void __launch_bounds__(THREADS)
 basp_relayout_kernel(const __grid_constant__ Params p) {
 #if BASP_PDL
     // Launched with programmatic stream serialisation: the previous kernel on
@@ -313,12 +325,12 @@ basp_relayout_kernel(const __grid_constant__ Params p) {
     // next kernel start its own launch.  The tile is located again after the
     // wait, so nothing stays live across it.
     if (blockIdx.x < p.prefetch_ctas && blockIdx.x < p.total_tiles)
-        prefetch_tile<VEC>(locate(p, blockIdx.x));
+        prefetch_tile<VEC, THREADS>(locate<THREADS>(p, blockIdx.x));
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" :::);
 #endif
     for (uint32_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x)
-        copy_tile<VEC>(locate(p, t));
+        copy_tile<VEC, THREADS>(locate<THREADS>(p, t));
 }
 
 }  // namespace
