@@ -98,3 +98,15 @@ def test_full_size_fp8(name, layout):
 @pytest.mark.parametrize("layout", ["basp", "ulysses"])
 def test_full_size_fp16(layout):
     _check(WORKLOADS["llama3.2-1b_B2_S8192"], "fp16", layout)
+
+
+@pytest.mark.parametrize("layout", ["basp", "ulysses"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_long_launch_ragged_tiles(layout, dtype):
+    """A launch long enough for the 512-thread CTAs on 32 KiB tiles (about
+    22K tiles of 16 KiB for Q, K, V), with S/K = 4098 tokens per block (the
+    last tile of every block is ragged) and d = 136 (rows of 102 or 51
+    vectors, not a power of two)."""
+    from sequence_re_layout_gb300.workloads import Workload
+    w = Workload("long_ragged", 2, 16392, 24, 8, 136, 8, 4)
+    _check(w, dtype, layout, kind="bits", seed=4242)
