@@ -8,6 +8,7 @@ module only allocates the outputs with torch and routes the gradients.
     L = basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16")
     q_h, k_h, v_h = seq2head(L, q, k, v)     # before attention
     o_s = head2seq(L, o_h)                   # after attention
+    q_h, k_h, v_h = seq2head_qkv(L, qkv)     # from a fused QKV projection
 
 Inputs are virtual-rank buffers (flat, or any contiguous shape with the right
 number of elements); outputs are flat tensors of the same dtype and device.
@@ -76,3 +77,38 @@ def head2seq(layout, o):
     """head-sharded attention output O (Hq heads) -> seq-sharded,
     differentiable."""
     return _Head2Seq.apply(layout, o)
+
+
+class _Seq2HeadQKV(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, layout, qkv):
+        ctx.layout = layout
+        qkv = qkv.contiguous()
+        ctx.packed_shape = qkv.shape
+        esz = qkv.element_size()
+        i = layout.info
+        outs = [torch.empty(n // esz, dtype=qkv.dtype, device=qkv.device)
+                for n in (i["bytes_q"], i["bytes_kv"], i["bytes_kv"])]
+        binding.basp_seq2head_qkv(layout.handle, qkv, *outs, stream=_stream())
+        return tuple(outs)
+
+    @staticmethod
+    def backward(ctx, dq, dk, dv):
+        i = ctx.layout.info
+        ref = next(g for g in (dq, dk, dv) if g is not None)
+        esz = ref.element_size()
+        # the packed gradient has every head range: a missing one is zero
+        grads = [torch.zeros(n // esz, dtype=ref.dtype, device=ref.device) if g is None
+                 else g.contiguous()
+                 for g, n in zip((dq, dk, dv), (i["bytes_q"], i["bytes_kv"], i["bytes_kv"]))]
+        out = torch.empty(ctx.packed_shape, dtype=ref.dtype, device=ref.device)
+        binding.basp_head2seq_qkv(ctx.layout.handle, *grads, out, stream=_stream())
+        return None, out
+
+
+def seq2head_qkv(layout, qkv):
+    """seq-sharded packed QKV (each token row holds the Hq query heads, then
+    the Hkv key heads, then the Hkv value heads: a fused QKV projection's
+    output) -> head-sharded Q, K, V, differentiable.  The backward packs the
+    three gradients into one seq-sharded gradient of the packed input."""
+    return _Seq2HeadQKV.apply(layout, qkv)

@@ -135,7 +135,7 @@ def _current_device() -> int:
     return torch.cuda.current_device()
 
 
-def _tptr(x, need, where, name, place):
+def _tptr(x, need, where, name, place, cur=None):
     """Address of a buffer argument.  Raw ints pass through unchecked; a tensor
     must be contiguous, hold at least `need` bytes, and live where the call
     reads it: "device" (a CUDA tensor on the current device, or page-locked
@@ -153,7 +153,8 @@ def _tptr(x, need, where, name, place):
             # the library launches on the current device (and takes its
             # built-in scratch there), so a tensor on another GPU would be
             # reached across devices: refuse it
-            cur = _current_device()
+            if cur is None:
+                cur = _current_device()
             if x.device.index != cur:
                 raise ValueError("%s: %s is on cuda:%s but the current device is "
                                  "cuda:%d; make its device current first"
@@ -170,7 +171,11 @@ def _triple(layout, where, names, bufs, place):
     """Check the (Hq, Hkv, Hkv) buffer triple of one call."""
     i = _info(layout)
     need = (i["bytes_q"], i["bytes_kv"], i["bytes_kv"]) if i else (None,) * 3
-    return [_tptr(b, n, where, nm, place) for b, n, nm in zip(bufs, need, names)]
+    # the current device, asked once for the whole triple
+    cur = None
+    if place == "device" and any(getattr(b, "is_cuda", False) for b in bufs):
+        cur = _current_device()
+    return [_tptr(b, n, where, nm, place, cur) for b, n, nm in zip(bufs, need, names)]
 
 
 def _stream(s):

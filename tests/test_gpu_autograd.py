@@ -57,3 +57,31 @@ def test_only_q_and_unused_outputs():
         kh.float().sum().backward()
         assert q.grad is None or torch.count_nonzero(q.grad) == 0
         assert torch.equal(k.grad, torch.ones_like(k))
+
+
+@pytest.mark.parametrize("K", [4, 8])
+def test_packed_qkv_forward_and_gradient(K):
+    """seq2head_qkv: the head-sharded Q, K, V of a packed projection output,
+    and the packed gradient (head2seq of each gradient, packed) -- with all
+    three outputs used, and with only Q used (K and V gradients are zero)."""
+    from sequence_re_layout_gb300.autograd import seq2head_qkv
+    B, S, Hq, Hkv, d, N = 2, 256, 32, 8, 64, 8
+    nq, nkv = B * S * Hq * d, B * S * Hkv * d
+    with basp.Layout(B, S, Hq, Hkv, d, N, K, "bf16") as L:
+        qkv = synth_inputs.normal(nq + 2 * nkv, 21, "bf16").to(DEV).requires_grad_()
+        qh, kh, vh = seq2head_qkv(L, qkv)
+        want = oracle.seq2head_qkv(_bits(qkv), B, S, Hq, Hkv, d, N, K)
+        for got, e in zip((qh, kh, vh), want):
+            assert np.array_equal(_bits(got), e)
+        gq, gk, gv = (synth_inputs.normal(n, s, "bf16").to(DEV)
+                      for n, s in ((nq, 22), (nkv, 23), (nkv, 24)))
+        torch.autograd.backward([qh, kh, vh], [gq, gk, gv])
+        assert np.array_equal(_bits(qkv.grad), oracle.head2seq_qkv(
+            _bits(gq), _bits(gk), _bits(gv), B, S, Hq, Hkv, d, N, K))
+
+        qkv.grad = None
+        qh, kh, vh = seq2head_qkv(L, qkv)
+        qh.backward(gq)
+        zeros = np.zeros(nkv, dtype=_bits(gq).dtype)
+        assert np.array_equal(_bits(qkv.grad), oracle.head2seq_qkv(
+            _bits(gq), zeros, zeros, B, S, Hq, Hkv, d, N, K))
