@@ -28,16 +28,20 @@
 // identity pass skipped on request when BYDST and HEAD address rows alike.
 // Packed QKV input is three jobs whose SEQ rows stride over the packed row.
 //
-// Launch policy (all measured on GB300): one 16 KiB tile per CTA rather than
-// a persistent grid (5-12% faster on HBM: retiring CTAs let new ones start
-// their loads while others drain their stores), except for page-locked host
-// buffers, where a persistent grid of one CTA per SM moves the most over the
-// host link; programmatic dependent launch, so a kernel's CTAs may be scheduled
-// while the previous kernel on the stream drains (each waits with
-// griddepcontrol.wait before touching memory), hiding the launch gap between
-// back-to-back re-layouts (3-10% per step); and an L2 prefetch of each CTA's
-// tile before that wait, which overlaps the first DRAM reads of a launch with
-// the previous one's tail (+1% per step at S=32768, +18% at S=1024).
+// Launch policy (all measured on GB300):
+//   - one tile per CTA rather than a persistent grid (5-12% faster on HBM:
+//     retiring CTAs let new ones start their loads while others drain their
+//     stores): 16 KiB tiles of 256 threads, and 32 KiB tiles of 512 threads
+//     for launches of at least 8 waves (+0.4-0.8% there);
+//   - page-locked host buffers instead take a persistent grid of one
+//     256-thread CTA per SM, which moves the most over the host link;
+//   - programmatic dependent launch, so a kernel's CTAs may be scheduled while
+//     the previous kernel on the stream drains (each waits with
+//     griddepcontrol.wait before touching memory), hiding the launch gap
+//     between back-to-back re-layouts (3-10% per step);
+//   - an L2 prefetch of each CTA's tile before that wait, which overlaps the
+//     first DRAM reads of a launch with the previous one's tail (+1% per step
+//     at S=32768, +18% at S=1024).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
