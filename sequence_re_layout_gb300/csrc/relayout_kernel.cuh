@@ -2,16 +2,16 @@
 // every pass launches, its job table and its load/store helpers.  Included
 // once, by relayout.cu.
 //
-// Each CTA copies one tile of THREADS * kUnroll vectors (16 KiB at 16-byte
-// vectors and 256 threads; 32 KiB with the 512-thread CTAs of long launches).  A tile lies inside one block of rows (fixed g, j, jp, bl); the
-// block's source and destination bases come from its four digits times the
-// job's stride tables, and vector i of the block sits in row i / vpr,
-// column i % vpr.  Loads are non-coherent and skip L1; stores are plain
-// (the written lines stay in L2 at normal priority).  Every thread issues
-// its kUnroll loads before its stores.
-// Every CTA first prefetches its tile's source lines into L2; the ones
-// resident before the previous kernel on the stream has finished do so while
-// it drains, before they wait for it.
+// Each CTA copies one tile of THREADS * kUnroll vectors: 16 KiB at 16-byte
+// vectors and 256 threads, 32 KiB with the 512-thread CTAs of long launches.
+// A tile lies inside one block of rows (fixed g, j, jp, bl); the block's
+// source and destination bases come from its four digits times the job's
+// stride tables, and vector i of the block sits in row i / vpr, column
+// i % vpr.  Loads are non-coherent and skip L1; stores are plain (the written
+// lines stay in L2 at normal priority).  Every thread issues its kUnroll
+// loads before its stores.  Every CTA first prefetches its tile's source
+// lines into L2; the ones resident before the previous kernel on the stream
+// has finished do so while it drains, before they wait for it.
 #pragma once
 
 #include <cuda_runtime.h>
