@@ -801,6 +801,14 @@ def main_ours(args, dist):
                             % args.window_ms),
         "timing_check": head["check"],
         "distribution": head["distribution"],
+        "context": {
+            "pages_figures": "BASP vs Ulysses in training: 1.17-1.31x end-to-end step "
+                             "speedup and 2.23-3.10x less all-to-all time (six Llama/Qwen "
+                             "models, S=16K, B=2, N=8)",
+            "pages_hardware": "2 nodes x 4 NVIDIA A100-40GB, 400 Gb/s InfiniBand, "
+                              "modified DeepSpeed",
+            "note": "the pages publish no GB/s for the re-layout itself; these are "
+                    "context, not a baseline for this line"},
         "analytic": {"peers_per_rank": info["peers"],
                      "bytes_per_peer_q": info["bytes_per_peer_q"],
                      "bytes_per_peer_kv": info["bytes_per_peer_kv"],

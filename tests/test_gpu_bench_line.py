@@ -33,6 +33,8 @@ def test_default_line_has_the_contract_fields():
     assert d["config"]["workload"] == "llama3.2-3b_B2_S32768"
     r = d["roofline"]
     assert r["bound"] == "hbm" and 0 < r["frac"] < 1.5 and r["achieved"] > 0
+    # the pages' own figures ride along as context, with their hardware
+    assert "A100" in d["context"]["pages_hardware"]
     # a distribution over 30 step windows
     dd = d["distribution"]
     assert dd["windows"] == 30 and dd["gbs_p10"] <= dd["gbs_median"] <= dd["gbs_p90"]
