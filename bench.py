@@ -799,7 +799,8 @@ def main_ours(args, dist):
                        note="the same step over a window of >= %g ms, after the "
                             "timed region; `value` is the timed region alone"
                             % args.window_ms),
-        "timing_check": head["check"],
+        "timing_check": dict(head["check"], ratio_vs_timed_region=round(
+            (r["s2h_ms_mean"] + r["h2s_ms_mean"]) / (t_max / args.steps), 4)),
         "distribution": head["distribution"],
         "context": {
             "pages_figures": "BASP vs Ulysses in training: 1.17-1.31x end-to-end step "

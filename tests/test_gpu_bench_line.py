@@ -42,6 +42,7 @@ def test_default_line_has_the_contract_fields():
     assert r["copy_same_run"]["gbs"] > 1000
     # the per-kernel times add up to the step time
     assert d["timing_check"]["consistent"] and d["timing_check"]["plausible"]
+    assert 0.9 < d["timing_check"]["ratio_vs_timed_region"] < 1.1
     c = d["cpu_baseline"]
     assert set(("value", "unit", "cores", "kind", "sample")) <= set(c)
     assert c["threads_1"]["value"] > 0 and c["threads_all"]["threads"] == c["cores"] >= 1
