@@ -860,6 +860,17 @@ def main_ours(args, dist):
                       "seq2head": lu["seq2head"], "head2seq": lu["head2seq"],
                       "steady": lu["steady_step"], "timing_check": lu["check"]}
         launches_total += ru["total_launches"]
+        basp_r, uly_r = (r, ru) if args.layout == "basp" else (ru, r)
+        out["basp_vs_ulysses"] = {
+            "step_time_ratio": round(uly_r["steady_ms_per_step"] / basp_r["steady_ms_per_step"], 4),
+            "peers_per_rank": {"basp": basp_r["info"]["peers"], "ulysses": uly_r["info"]["peers"]},
+            "remote_bytes_per_rank": {
+                lay: rr["info"]["peers"] * (rr["info"]["bytes_per_peer_q"] +
+                                            2 * rr["info"]["bytes_per_peer_kv"])
+                for lay, rr in (("basp", basp_r), ("ulysses", uly_r))},
+            "note": "Ulysses step time over BASP's (steady windows). On one GPU both layouts "
+                    "move the same bytes; BASP's rows are B times longer. The pages' gain "
+                    "comes from keeping the K-way exchange inside a node."}
         legs = {(w.name, args.layout): head, (w.name, other): lu}
         if args.layout == "basp" and w.N % w.B == 0:
             # the review's "trivial alternative" (Strengths, Table I): Ulysses

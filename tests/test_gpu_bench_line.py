@@ -33,6 +33,9 @@ def test_default_line_has_the_contract_fields():
     assert d["config"]["workload"] == "llama3.2-3b_B2_S32768"
     r = d["roofline"]
     assert r["bound"] == "hbm" and 0 < r["frac"] < 1.5 and r["achieved"] > 0
+    # BASP against Ulysses on the same shape: peers K-1 = 3 against N-1 = 7
+    bu = d["basp_vs_ulysses"]
+    assert bu["peers_per_rank"] == {"basp": 3, "ulysses": 7} and bu["step_time_ratio"] > 0.9
     # the pages' own figures ride along as context, with their hardware
     assert "A100" in d["context"]["pages_hardware"]
     # a distribution over 30 step windows
